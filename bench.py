@@ -1,0 +1,412 @@
+"""Benchmark: per-token logprob + entropy + weighted backward at V = 151,936.
+
+One step is one pass of the hot path over one batch: pstat_forward (chunk
+statistics + fixed-order combine) and pstat_backward (fused weighted
+gradient, bf16 dlogits) on T = 8192 rows of bf16 logits N(0, 2^2), labels
+sampled from each row's softmax, weights N(0, 1) x a 0/1 mask with 20% zeros.
+
+Prints ONE JSON line (rank 0).  `value` is whole-job tokens/s with inputs
+resident in HBM; `e2e` is the same metric through the Python/C-ABI calls with
+the inputs copied from pinned host memory and logprob/entropy copied back
+inside the timed region; `roofline` is the dominant kernel's algorithmic
+bytes per launch over its CUDA-event duration against the measured HBM copy
+bandwidth; `cpu_baseline` times the float64 oracle on the host cores over a
+bounded sample of the same workload.
+
+`--impl reference` times the oracle alone (the reference arm): each step is a
+bounded sample of the same workload on the host cores.
+
+Multi-GPU (torchrun): tokens are independent rows, so each rank processes its
+own batch with no data-path collective (weak scaling); only the timing uses a
+barrier and a MAX reduction.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tokens/s and HBM GB/s (% of roofline) for logprob+entropy+bwd at V=151936"
+V = 151936
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--tokens", type=int, default=8192, help="rows per rank (profiling: smaller)")
+    p.add_argument("--cpu-rows", type=int, default=256, help="oracle sample rows")
+    p.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline")
+    p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
+    p.add_argument("--no-lmhead", action="store_true", help="skip the fused lm_head variant")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), float(pk["bf16_tflops"]), float(pk["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.proc = None
+        self.idx = gpu_index
+        self.window = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        t0, t1 = self.window or (0, 1e30)
+        inside = [s for t, s in self.samples if t0 <= t <= t1]
+        if not inside:  # timed region shorter than the sampling period: nearest samples
+            mid = (t0 + t1) / 2
+            inside = [min(self.samples, key=lambda ts: abs(ts[0] - mid))[1]]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in inside:
+            f = [x.strip() for x in line.split(",")]
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+def oracle_sample(rows: int, seed: int = 2):
+    """A bounded sample of the workload drawn on the host (same law)."""
+    import torch
+    from vocab_wide_token_gb300 import inputs
+
+    d = inputs.fwdbwd_workload(seed, "cpu", T=rows)
+    z = d["logits"].contiguous().view(torch.int16).numpy().view("uint16")
+    return z, d["labels"].numpy(), d["weights"].double().numpy()
+
+
+def time_oracle(z, y, w):
+    import oracle
+
+    t0 = time.perf_counter()
+    oracle.forward(z, y, -100)
+    oracle.backward(z, y, w, -100)
+    return time.perf_counter() - t0, oracle.threads()
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    rows = args.cpu_rows
+    z, y, w = oracle_sample(rows)
+    for _ in range(args.warmup):
+        time_oracle(z, y, w)
+    t = 0.0
+    cores = oracle.threads()
+    for _ in range(args.steps):
+        dt, cores = time_oracle(z, y, w)
+        t += dt
+    tok_s = rows * args.steps / t
+    sample = f"{rows} rows of the fwdbwd workload (V={V}, bf16) per step, forward+backward"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tok_s, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"fwdbwd bounded sample: {rows} rows x V={V} bf16 logits",
+                   "global_batch": rows, "seq_len": None, "parallelism": "host cores"},
+        "cpu_baseline": {"value": tok_s, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": tok_s, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def traffic_record(kernel: str):
+    """dram bytes per launch recorded by ncu, if the kernel source is unchanged."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    src = os.path.join(ROOT, "vocab_wide_token_gb300", "csrc", "stats_kernels.cu")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[kernel]
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        if rec.get("source_sha256") != sha:
+            return None, None
+        return float(rec["dram_bytes_per_launch"]), float(rec.get("rows", 0))
+    except Exception:
+        return None, None
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    from vocab_wide_token_gb300 import inputs, pstat
+
+    T = args.tokens
+    d = inputs.fwdbwd_workload(2 + 1000 * rank, dev, T=T)
+    z, y, w = d["logits"], d["labels"], d["weights"]
+    err = pstat.new_error_flag(dev)
+    lp = torch.empty(T, dtype=torch.float32, device=dev)
+    ent = torch.empty(T, dtype=torch.float32, device=dev)
+    rs = torch.empty(T, 2, dtype=torch.float32, device=dev)
+    g = torch.empty(T, V, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(pstat.workspace_size(T, V, torch.bfloat16), dtype=torch.uint8, device=dev)
+    active_rows = int(((w != 0) & (y != -100)).sum().item())
+
+    def step():
+        pstat.forward(z, y, -100, None, out=(lp, ent, rs), workspace=ws, dev_error=err)
+        pstat.backward(z, y, w, rs, -100, out=g, dev_error=err)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    # ---- timed region: device-resident inputs -------------------------------
+    stream = torch.cuda.current_stream(dev)
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    t_wall0 = time.time()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for k in range(K):
+        ev[k][0].record(stream)
+        pstat.forward(z, y, -100, None, out=(lp, ent, rs), workspace=ws, dev_error=err)
+        ev[k][1].record(stream)
+        pstat.backward(z, y, w, rs, -100, out=g, dev_error=err)
+        ev[k][2].record(stream)
+    end.record(stream)
+    barrier()
+    t_wall1 = time.time()
+    clocks.window = (t_wall0, t_wall1)
+    time.sleep(0.25)
+    clocks.stop()
+    ms = start.elapsed_time(end)
+    fwd_ms = sum(ev[k][0].elapsed_time(ev[k][1]) for k in range(K)) / K
+    bwd_ms = sum(ev[k][1].elapsed_time(ev[k][2]) for k in range(K)) / K
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    assert err.item() == 0, f"device error bits {err.item()}"
+    ms_step = ms / K
+    tok_s = world * T * K / (ms / 1e3)
+
+    # algorithmic bytes (reads of rows whose gradient is identically zero are
+    # not needed: ignored rows and zero weights write +0.0 without reading)
+    fwd_bytes = T * (2 * V + 8 + 16)                 # logits, label, logprob/entropy/rowstats
+    bwd_bytes = active_rows * 2 * V + T * (2 * V + 20)  # read active rows, write every row
+    hbm, tflops, tflops_sus, peak_kind = measured_peaks()
+    bwd_gbs = bwd_bytes / (bwd_ms / 1e3) / 1e9
+    fwd_gbs = fwd_bytes / (fwd_ms / 1e3) / 1e9
+    step_gbs = (fwd_bytes + bwd_bytes) / (ms_step / 1e3) / 1e9
+    dominant = "backward_kernel" if bwd_ms >= fwd_ms else "chunk_stats_kernel"
+    traffic, traffic_rows = traffic_record(dominant)
+    if traffic is not None and traffic_rows:
+        traffic = traffic * T / traffic_rows
+    roof = {"bound": "hbm", "kernel": dominant,
+            "achieved": bwd_gbs if dominant == "backward_kernel" else fwd_gbs,
+            "peak": hbm, "unit": "GB/s", "peak_kind": peak_kind,
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": bwd_bytes if dominant == "backward_kernel" else fwd_bytes}
+    roof["frac"] = roof["achieved"] / hbm
+
+    line = {
+        "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"fwdbwd: T={T} rows per GPU x V={V} bf16 logits N(0,2^2), "
+                               "sampled labels, weights N(0,1) x mask(20% zero), bf16 dlogits",
+                   "global_batch": T * world, "seq_len": None, "parallelism": f"dp{world}",
+                   "l2": "inputs larger than L2 (2.49 GB logits per rank)"},
+        "gbs": step_gbs,
+        "kernels": {"forward_ms": fwd_ms, "forward_gbs": fwd_gbs, "forward_frac": fwd_gbs / hbm,
+                    "backward_ms": bwd_ms, "backward_gbs": bwd_gbs, "backward_frac": bwd_gbs / hbm,
+                    "active_rows": active_rows},
+        "roofline": roof,
+        "gpu_launches": 3 * K,
+        "clocks": clocks.summary(),
+    }
+
+    # ---- e2e: host buffers through the public API ---------------------------
+    if not args.no_e2e:
+        zh = z.cpu().pin_memory()
+        yh = y.cpu().pin_memory()
+        wh = w.cpu().pin_memory()
+        outh = torch.empty(2, T, dtype=torch.float32).pin_memory()
+        zd = torch.empty_like(z)
+        yd = torch.empty_like(y)
+        wd = torch.empty_like(w)
+        Ke = min(K, 20)
+
+        def e2e_step():
+            zd.copy_(zh, non_blocking=True)
+            yd.copy_(yh, non_blocking=True)
+            wd.copy_(wh, non_blocking=True)
+            pstat.forward(zd, yd, -100, None, out=(lp, ent, rs), workspace=ws, dev_error=err)
+            pstat.backward(zd, yd, wd, rs, -100, out=g, dev_error=err)
+            outh[0].copy_(lp, non_blocking=True)
+            outh[1].copy_(ent, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        s2 = torch.cuda.Event(enable_timing=True)
+        e2 = torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for _ in range(Ke):
+            e2e_step()
+        e2.record(stream)
+        barrier()
+        ms2 = s2.elapsed_time(e2)
+        if world > 1:
+            t = torch.tensor([ms2], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ms2 = float(t.item())
+        line["e2e"] = {"value": world * T * Ke / (ms2 / 1e3), "unit": "tokens/s",
+                       "h2d_bytes_per_step": zh.numel() * 2 + yh.numel() * 8 + wh.numel() * 4,
+                       "d2h_bytes_per_step": outh.numel() * 4, "steps": Ke}
+        del zh, zd
+
+    # ---- fused lm_head variant (rank 0 reports) ------------------------------
+    if not args.no_lmhead:
+        line["lmhead"] = bench_lmhead(pstat, dev, tflops, tflops_sus, peak_kind)
+
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N=1 only) ------
+    if rank == 0 and world == 1 and not args.no_cpu:
+        import oracle
+        oracle.build()
+        rows = args.cpu_rows
+        zs, ys, ws_ = oracle_sample(rows)
+        dt, cores = time_oracle(zs, ys, ws_)
+        line["cpu_baseline"] = {"value": rows / dt, "unit": "tokens/s", "cores": cores,
+                                "kind": "oracle",
+                                "sample": f"{rows} rows of the same workload law (V={V}, bf16), "
+                                          "float64 forward+backward, one pass"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def bench_lmhead(pstat, dev, tflops, tflops_sus, peak_kind, steps=5, warmup=2):
+    """Fused lm_head statistics on hidden [16384, 4096] x W [151936, 4096] bf16
+    (the tcgen05 GEMM with the statistics epilogue + the combine kernel)."""
+    import torch
+    from vocab_wide_token_gb300 import inputs
+
+    try:
+        pstat.lmhead_workspace_size(16, V, 4096)
+    except pstat.PstatError as e:
+        return {"status": f"unavailable: {e}"}
+    d = inputs.lmhead_workload(4, dev)
+    h, W, y = d["hidden"], d["W"], d["labels"]
+    T, dm = h.shape
+    err = pstat.new_error_flag(dev)
+    ws = torch.empty(pstat.lmhead_workspace_size(T, V, dm), dtype=torch.uint8, device=dev)
+    for _ in range(warmup):
+        pstat.lmhead_forward(h, W, y, -100, workspace=ws, dev_error=err)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        pstat.lmhead_forward(h, W, y, -100, workspace=ws, dev_error=err)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    assert err.item() == 0, f"device error bits {err.item()}"
+    flop = 2.0 * T * V * dm
+    achieved = flop / (ms / 1e3) / 1e12
+    return {"status": "ok", "workload": f"hidden [{T}, {dm}] x W [{V}, {dm}] bf16",
+            "forward_ms": ms, "forward_tokens_per_s": T / (ms / 1e3),
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": tflops,
+                         "unit": "TFLOP/s", "frac": achieved / tflops, "peak_kind": peak_kind,
+                         "traffic": None},
+            "gpu_launches_per_call": 2}
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,190 @@
+/*
+ * pstat.h -- C ABI of libpstat.so: batch-invariant per-token policy
+ * statistics over a wide vocabulary on one GB300 (sm_103a).
+ *
+ * What the library computes is defined in torchtitan PR #4685, "[RL] Avoid
+ * full-vocab gather for TP policy statistics":
+ *   - Summary / Why: per-token sampled-token logprob and exact entropy from
+ *     shard-local sufficient statistics (global maximum, softmax
+ *     denominator, target contribution, entropy-weighted sum); entropy is a
+ *     no-grad metric.
+ *   - Review diff of loss.py: logprobs = -cross_entropy(logits, labels).
+ *   - Correctness and compatibility: even/uneven vocabulary shards, FP32 and
+ *     BF16 logits, ignored labels, partially masked (-inf) logits, and
+ *     non-uniformly weighted gradients compared with the full vocabulary.
+ * The fused lm_head entry points follow the chunked lm_head of TRL PR #6949
+ * "ZeroSyncGRPOTrainer" (the vocabulary projection is multiplied chunk by
+ * chunk; backward GEMMs run in bf16 and accumulate in fp32).
+ *
+ * Per row t with logits z_t[0..V), label y_t and weight w_t:
+ *   M_t       = max_v z_tv,   S_t = sum_v exp(z_tv - M_t)
+ *   logprob_t = z_{t,y_t} - M_t - ln S_t          (+0.0 if y_t == ignore_index)
+ *   entropy_t = ln S_t - U_t / S_t,  U_t = sum_v exp(z_tv - M_t)(z_tv - M_t)
+ *               (computed for ignored rows too: it does not depend on y_t)
+ *   dlogits_tv = w_t (1[v = y_t] - exp(z_tv - M_t - ln S_t))
+ *               (an all +0.0 row when y_t == ignore_index or w_t == 0)
+ *
+ * Numerics and batch invariance.  Each row is cut into fixed chunks that
+ * restart at every shard start: chunk k of shard s covers columns
+ * [b_s + k C, min(b_s + (k+1) C, b_{s+1})), C = PSTAT_CHUNK_BF16 or
+ * PSTAT_CHUNK_F32 elements.  Per chunk the kernel forms (m, s, u) with a
+ * reduction tree fixed at compile time; chunks are folded in ascending order
+ * within a shard and shards in ascending order within the row.  A row's
+ * results therefore depend only on its own values, V, the shard bounds and
+ * the dtype: they are bit-identical whatever batch the row sits in, at
+ * whatever position, and from call to call.  Sharded and unsharded results
+ * agree to rounding, not bitwise (the page's point that a partial sum then a
+ * SUM reduction differs in the low bits from one contiguous sum).
+ *
+ * Conventions for every entry point:
+ *   - All pointers except `shard_bounds` are DEVICE pointers owned by the
+ *     caller (typically torch tensors).  `shard_bounds` is a HOST array.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  The library allocates no memory; scratch lives in the
+ *     caller's `workspace`, sized by the matching *_workspace_size call.
+ *   - Errors a host can see (null pointers, shapes, shard bounds, dtype,
+ *     alignment, workspace size) are returned before anything is launched.
+ *     A launch failure returns PSTAT_ERR_CUDA (from cudaGetLastError).
+ *   - Errors only the device can see are OR-ed into `*dev_error` (a device
+ *     int, may be NULL) with atomics, and the affected row's outputs become
+ *     NaN; no kernel traps or asserts.  Read the flag when you need it.
+ *   - Labels are int64, weights float32, statistics and logprob/entropy
+ *     float32.  Logits/dlogits are row-major with a row stride `ld` (in
+ *     elements, >= V).
+ */
+#ifndef PSTAT_H
+#define PSTAT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PSTAT_API __attribute__((visibility("default")))
+#else
+#define PSTAT_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA stream handle; identical to cudaStream_t. */
+typedef struct CUstream_st* pstat_stream_t;
+
+typedef enum { PSTAT_F32 = 0, PSTAT_BF16 = 1 } pstat_dtype;
+
+/* Return codes. */
+enum {
+    PSTAT_OK = 0,
+    PSTAT_ERR_NULLPTR = -1,     /* a required pointer is NULL */
+    PSTAT_ERR_SHAPE = -2,       /* T < 0, V < 1, ld < V, d not a multiple of 64, ... */
+    PSTAT_ERR_SHARDS = -3,      /* bounds not strictly increasing from 0 to V, or too many */
+    PSTAT_ERR_DTYPE = -4,       /* unknown dtype or unsupported combination */
+    PSTAT_ERR_ALIGN = -5,       /* a pointer lacks the alignment stated for it */
+    PSTAT_ERR_WORKSPACE = -6,   /* workspace NULL or smaller than required */
+    PSTAT_ERR_CUDA = -7,        /* a CUDA runtime call or launch failed */
+    PSTAT_ERR_UNSUPPORTED = -8  /* the current device is not sm_103 (GB300) */
+};
+
+/* Bits OR-ed into *dev_error by the kernels. */
+#define PSTAT_DEV_BAD_LABEL 0x1 /* label outside [0, V) and != ignore_index */
+#define PSTAT_DEV_EMPTY_ROW 0x2 /* every logit of a row is -inf: softmax undefined */
+#define PSTAT_DEV_TIMEOUT 0x4   /* a bounded wait on an asynchronous copy gave up */
+
+#define PSTAT_MAX_SHARDS 64
+#define PSTAT_CHUNK_BF16 4096 /* chunk length in elements for bf16 logits */
+#define PSTAT_CHUNK_F32 2048  /* chunk length in elements for fp32 logits */
+
+/* Human-readable text for a return code; never NULL. */
+PSTAT_API const char* pstat_status_string(int code);
+
+/* Version of this ABI (major * 10000 + minor * 100 + patch). */
+PSTAT_API int pstat_version(void);
+
+/*
+ * Workspace bytes for pstat_forward / pstat_backward on T rows of V logits
+ * of dtype `dt` split by `shard_bounds` (host, n_shards + 1 entries; NULL and
+ * n_shards = 1 mean one shard {0, V}).  The workspace holds one 16-byte
+ * (m, s, u) record per row and chunk, and the (M, ln S) pair per row that
+ * pstat_backward needs when it is not given `rowstats`.
+ */
+PSTAT_API int pstat_workspace_size(int64_t T, int64_t V, pstat_dtype dt, const int64_t* shard_bounds,
+                         int n_shards, size_t* bytes);
+
+/*
+ * Forward statistics (chunk-statistics kernel, then the fixed-order combine).
+ *   logits        [T, ld] dtype `dt`; element (t, v) at logits + t*ld + v.
+ *                 Any alignment works; 16-byte aligned rows and chunk starts
+ *                 take the bulk-copy path, others a slower path with the same
+ *                 numerics.
+ *   labels        [T] int64 (NULL: every row ignored).
+ *   shard_bounds  host int64[n_shards + 1], 0 = b_0 < b_1 < ... < b_S = V,
+ *                 n_shards <= PSTAT_MAX_SHARDS; NULL means {0, V}.
+ *   out_logprob   [T] float (may be NULL), out_entropy [T] float (may be
+ *                 NULL), out_rowstats [T, 2] float (M, ln S) (may be NULL).
+ *   workspace     >= pstat_workspace_size(...) bytes, 16-byte aligned.
+ *   dev_error     device int or NULL; bits PSTAT_DEV_*.
+ * T = 0 is a no-op returning PSTAT_OK.
+ */
+PSTAT_API int pstat_forward(const void* logits, pstat_dtype dt, int64_t T, int64_t V, int64_t ld,
+                  const int64_t* labels, int64_t ignore_index, const int64_t* shard_bounds,
+                  int n_shards, float* out_logprob, float* out_entropy, float* out_rowstats,
+                  void* workspace, size_t ws_bytes, int* dev_error, pstat_stream_t stream);
+
+/*
+ * Weighted backward dlogits = w (onehot(y) - softmax(z)) (fused elementwise
+ * kernel).
+ *   weights       [T] float (NULL: all ones).
+ *   rowstats      [T, 2] float (M, ln S) from pstat_forward on the same
+ *                 logits and shard bounds; NULL recomputes them first through
+ *                 the forward kernels (needs the workspace).
+ *   out_dlogits   [T, ld_out] of `out_dt` (PSTAT_BF16 rounds to nearest even;
+ *                 PSTAT_F32 needs dt == PSTAT_F32).  Every element of the
+ *                 T x V block is written.
+ *   workspace     needed only when rowstats is NULL (else may be NULL / 0).
+ */
+PSTAT_API int pstat_backward(const void* logits, pstat_dtype dt, int64_t T, int64_t V, int64_t ld,
+                   const int64_t* labels, int64_t ignore_index, const float* weights,
+                   const float* rowstats, const int64_t* shard_bounds, int n_shards,
+                   void* out_dlogits, pstat_dtype out_dt, int64_t ld_out, void* workspace,
+                   size_t ws_bytes, int* dev_error, pstat_stream_t stream);
+
+/*
+ * Workspace bytes for the fused lm_head entry points (T tokens, V vocab
+ * rows, hidden size d).
+ */
+PSTAT_API int pstat_lmhead_workspace_size(int64_t T, int64_t V, int64_t d, size_t* bytes);
+
+/*
+ * Fused lm_head forward: logits z = hidden W^T are formed tile by tile on
+ * the tensor cores (bf16 operands, fp32 accumulation in tensor memory) and
+ * folded straight into the chunk statistics; logits are never written to
+ * memory.  Outputs as pstat_forward.
+ *   hidden  [T, d] bf16 row-major, W [V, d] bf16 row-major; both 16-byte
+ *           aligned, d a multiple of 64 (PSTAT_ERR_SHAPE otherwise).
+ */
+PSTAT_API int pstat_lmhead_fused(const void* hidden, const void* W, int64_t T, int64_t V, int64_t d,
+                       const int64_t* labels, int64_t ignore_index, float* out_logprob,
+                       float* out_entropy, float* out_rowstats, void* workspace,
+                       size_t ws_bytes, int* dev_error, pstat_stream_t stream);
+
+/*
+ * Fused lm_head backward through z = hidden W^T of the weighted gradient
+ * g = w (onehot(y) - softmax(z)):
+ *   dhidden [T, d] float  += g W
+ *   dW      [V, d] float  += g^T hidden
+ * Both are ACCUMULATED into (zero them first for a plain gradient), so calls
+ * over token or vocabulary chunks compose.  rowstats [T, 2] from
+ * pstat_lmhead_fused is required.  g is formed on chip from recomputed
+ * logits and staged only per vocabulary chunk in the workspace.
+ */
+PSTAT_API int pstat_lmhead_backward(const void* hidden, const void* W, int64_t T, int64_t V, int64_t d,
+                          const int64_t* labels, int64_t ignore_index, const float* weights,
+                          const float* rowstats, float* dhidden, float* dW, void* workspace,
+                          size_t ws_bytes, int* dev_error, pstat_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PSTAT_H */

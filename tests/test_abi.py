@@ -1,0 +1,103 @@
+"""The C-ABI library loads, exports every symbol include/pstat.h declares, and
+rejects bad arguments before launching anything.  Runs without a GPU: every
+call here fails host-side validation (or, with valid arguments, fails to find
+a device), so no kernel is ever launched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pstat.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from vocab_wide_token_gb300 import build
+
+    if not os.path.exists(build.LIB):
+        try:
+            build.build()
+        except RuntimeError as e:  # no nvcc on this machine
+            pytest.skip(str(e))
+    from vocab_wide_token_gb300 import pstat
+
+    return pstat.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"PSTAT_API\s+[\w\s\*]+?\b(pstat_\w+)\s*\(", text)
+
+
+def test_header_declares_entry_points():
+    names = declared_symbols()
+    for must in ("pstat_forward", "pstat_backward", "pstat_lmhead_fused", "pstat_lmhead_backward",
+                 "pstat_workspace_size", "pstat_lmhead_workspace_size", "pstat_status_string",
+                 "pstat_version"):
+        assert must in names
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), f"libpstat.so does not export {name}"
+
+
+def test_status_strings(lib):
+    from vocab_wide_token_gb300 import pstat
+
+    for code in [0, -1, -2, -3, -4, -5, -6, -7, -8, 12345]:
+        s = lib.pstat_status_string(code)
+        assert isinstance(s, bytes) and len(s) > 0
+    assert pstat.version() >= 10000
+
+
+def _fwd(lib, logits=0x1000, dt=1, T=4, V=100, ld=100, bounds=None, ns=1, ws=0x2000,
+         ws_bytes=1 << 20, labels=0x3000):
+    b = None if bounds is None else (ctypes.c_int64 * len(bounds))(*bounds)
+    return lib.pstat_forward(ctypes.c_void_p(logits), dt, T, V, ld, ctypes.c_void_p(labels), -100,
+                             b, ns, None, None, None, ctypes.c_void_p(ws), ws_bytes, None, None)
+
+
+def test_forward_argument_checks(lib):
+    assert _fwd(lib, dt=7) == -4                       # dtype
+    assert _fwd(lib, V=0) == -2                        # shape
+    assert _fwd(lib, ld=99) == -2
+    assert _fwd(lib, T=-1) == -2
+    assert _fwd(lib, bounds=[0, 50, 40, 100], ns=3) == -3      # not increasing
+    assert _fwd(lib, bounds=[1, 50, 100], ns=2) == -3          # not starting at 0
+    assert _fwd(lib, bounds=[0, 50, 99], ns=2) == -3           # not ending at V
+    assert _fwd(lib, bounds=list(range(0, 66)) + [100], ns=66) == -3  # too many shards
+    assert _fwd(lib, T=0, logits=0) == 0               # empty batch is a no-op
+    assert _fwd(lib, logits=0) == -1                   # null logits
+    assert _fwd(lib, ws=0) == -6                       # no workspace
+    assert _fwd(lib, ws_bytes=16) == -6                # workspace too small
+    assert _fwd(lib, logits=0x1001) == -5              # bf16 logits must be 2-byte aligned
+    assert _fwd(lib, ws=0x2008) == -5                  # workspace must be 16-byte aligned
+    assert _fwd(lib, labels=0x3004) == -5
+
+
+def test_workspace_size(lib):
+    n = ctypes.c_size_t(0)
+    assert lib.pstat_workspace_size(8192, 151936, 1, None, 1, ctypes.byref(n)) == 0
+    # 38 chunks of 4096 per row, 16 bytes each, plus (M, ln S) per row, 256-aligned
+    assert n.value >= 8192 * 38 * 16 + 8192 * 8
+    b = (ctypes.c_int64 * 4)(0, 50000, 100000, 151936)
+    assert lib.pstat_workspace_size(8192, 151936, 1, b, 3, ctypes.byref(n)) == 0
+    assert n.value >= 8192 * 39 * 16
+    assert lib.pstat_workspace_size(10, 100, 5, None, 1, ctypes.byref(n)) == -4
+    assert lib.pstat_workspace_size(10, 100, 0, None, 1, None) == -1
+
+
+def test_backward_argument_checks(lib):
+    def bwd(dt=1, out_dt=1, T=4, V=100, ld=100, ld_out=100, logits=0x1000, out=0x4000,
+            rowstats=0x5000, ws=0, ws_bytes=0):
+        return lib.pstat_backward(ctypes.c_void_p(logits), dt, T, V, ld, None, -100, None,
+                                  ctypes.c_void_p(rowstats), None, 1, ctypes.c_void_p(out), out_dt,
+                                  ld_out, ctypes.c_void_p(ws), ws_bytes, None, None)
+    assert bwd(dt=1, out_dt=0) == -4       # bf16 logits cannot produce fp32 dlogits
+    assert bwd(ld_out=50) == -2
+    assert bwd(out=0) == -1
+    assert bwd(rowstats=0) == -6           # recompute needs a workspace
+    assert bwd(out=0x4001) == -5

@@ -1,0 +1,61 @@
+// internal.h -- declarations shared by the C-ABI layer and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/pstat.h"
+
+namespace pstat {
+
+// Fixed chunk plan of one row, identical for every row of a call: the chunks
+// restart at every shard start (so a shard's statistics are what a tensor-
+// parallel rank holding [b_s, b_{s+1}) would compute locally).
+struct ShardPlan {
+    int n_shards;
+    int n_chunks;                            // chunks per row
+    int chunk;                               // chunk length in elements
+    int cum[PSTAT_MAX_SHARDS + 1];           // first chunk index of each shard
+    int64_t bounds[PSTAT_MAX_SHARDS + 1];    // shard column bounds
+};
+
+// Builds the plan; returns PSTAT_OK or PSTAT_ERR_SHARDS.
+int make_plan(int64_t V, int chunk, const int64_t* bounds, int n_shards, ShardPlan* plan);
+
+constexpr size_t kChunkRecordBytes = 16;  // (m, s, u, unused) fp32
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Workspace layout of pstat_forward / pstat_backward.
+struct StatsWorkspace {
+    size_t chunk_stats_off;  // [T, n_chunks] float4
+    size_t rowstats_off;     // [T, 2] float
+    size_t total;
+};
+StatsWorkspace stats_workspace_layout(int64_t T, const ShardPlan& plan);
+
+// Device properties cached per device.
+struct DeviceInfo {
+    int sm_count;
+    int cc_major, cc_minor;
+    int max_smem_optin;
+};
+int device_info(DeviceInfo* info);  // PSTAT_OK / PSTAT_ERR_CUDA / PSTAT_ERR_UNSUPPORTED
+
+// Kernel launchers (stats_kernels.cu).  They assume validated arguments.
+cudaError_t launch_chunk_stats(const void* logits, pstat_dtype dt, int64_t T, int64_t ld,
+                               const ShardPlan& plan, float4* chunk_stats, int* dev_error,
+                               const DeviceInfo& dev, cudaStream_t stream);
+cudaError_t launch_combine(const float4* chunk_stats, const ShardPlan& plan, const void* logits,
+                           pstat_dtype dt, int64_t T, int64_t V, int64_t ld,
+                           const int64_t* labels, int64_t ignore_index, const float* target,
+                           float* logprob, float* entropy, float* rowstats, int* dev_error,
+                           cudaStream_t stream);
+cudaError_t launch_backward(const void* logits, pstat_dtype dt, int64_t T, int64_t V,
+                            int64_t ld, const int64_t* labels, int64_t ignore_index,
+                            const float* weights, const float* rowstats, void* out,
+                            pstat_dtype out_dt, int64_t ld_out, int* dev_error,
+                            const DeviceInfo& dev, cudaStream_t stream);
+
+}  // namespace pstat

@@ -1,0 +1,280 @@
+"""ctypes binding of libpstat.so (argument marshalling only).
+
+Every step of the computation runs in the CUDA kernels behind the C ABI
+declared in ``include/pstat.h``; this module turns torch tensors into device
+pointers, sizes and the current stream, allocates the workspace with torch,
+and raises on a non-zero status.  There is no CPU fallback: importing this
+module without a built ``libpstat.so`` raises, and every call needs CUDA
+tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpstat.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -m vocab_wide_token_gb300.build` "
+        "(nvcc, sm_103a); there is no fallback implementation")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+# ---- C ABI prototypes -------------------------------------------------------
+_i64, _i32, _vp, _sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+_lib.pstat_status_string.argtypes = [_i32]
+_lib.pstat_status_string.restype = ctypes.c_char_p
+_lib.pstat_version.restype = _i32
+_lib.pstat_workspace_size.argtypes = [_i64, _i64, _i32, _vp, _i32, ctypes.POINTER(_sz)]
+_lib.pstat_workspace_size.restype = _i32
+_lib.pstat_forward.argtypes = [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _i32, _vp, _vp, _vp,
+                               _vp, _sz, _vp, _vp]
+_lib.pstat_forward.restype = _i32
+_lib.pstat_backward.argtypes = [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _vp,
+                                _i32, _i64, _vp, _sz, _vp, _vp]
+_lib.pstat_backward.restype = _i32
+_lib.pstat_lmhead_workspace_size.argtypes = [_i64, _i64, _i64, ctypes.POINTER(_sz)]
+_lib.pstat_lmhead_workspace_size.restype = _i32
+_lib.pstat_lmhead_fused.argtypes = [_vp, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _vp,
+                                    _sz, _vp, _vp]
+_lib.pstat_lmhead_fused.restype = _i32
+_lib.pstat_lmhead_backward.argtypes = [_vp, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _vp,
+                                       _vp, _sz, _vp, _vp]
+_lib.pstat_lmhead_backward.restype = _i32
+
+F32, BF16 = 0, 1
+OK = 0
+ERR = {-1: "NULLPTR", -2: "SHAPE", -3: "SHARDS", -4: "DTYPE", -5: "ALIGN", -6: "WORKSPACE",
+       -7: "CUDA", -8: "UNSUPPORTED"}
+DEV_BAD_LABEL, DEV_EMPTY_ROW, DEV_TIMEOUT = 0x1, 0x2, 0x4
+CHUNK_BF16, CHUNK_F32 = 4096, 2048
+MAX_SHARDS = 64
+
+
+class PstatError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = _lib.pstat_status_string(code).decode()
+        super().__init__(f"{where}: {ERR.get(code, code)} ({msg})")
+
+
+def _check(code: int, where: str) -> None:
+    if code != OK:
+        raise PstatError(code, where)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (for callers that want the raw ABI)."""
+    return _lib
+
+
+def version() -> int:
+    return int(_lib.pstat_version())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"logits must be bfloat16 or float32, got {t.dtype}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _rows(logits: torch.Tensor):
+    if logits.dim() != 2:
+        raise ValueError("logits must be 2-D [T, V]")
+    if not logits.is_cuda:
+        raise ValueError("logits must be a CUDA tensor (no CPU path exists)")
+    if logits.stride(1) != 1:
+        raise ValueError("logits rows must be contiguous (stride(1) == 1)")
+    T, V = logits.shape
+    ld = logits.stride(0) if T > 1 else V
+    return T, V, ld
+
+
+def _bounds(shard_bounds, V):
+    if shard_bounds is None:
+        return None, 1
+    b = [int(x) for x in shard_bounds]
+    arr = (ctypes.c_int64 * len(b))(*b)
+    return arr, len(b) - 1
+
+
+def _labels(labels, T, device):
+    if labels is None:
+        return None
+    if labels.dtype != torch.int64 or labels.shape != (T,) or labels.device != device:
+        raise ValueError("labels must be int64 [T] on the logits' device")
+    return labels.contiguous()
+
+
+def workspace_size(T: int, V: int, dtype: torch.dtype, shard_bounds=None) -> int:
+    n = ctypes.c_size_t(0)
+    arr, ns = _bounds(shard_bounds, V)
+    code = BF16 if dtype == torch.bfloat16 else F32
+    _check(_lib.pstat_workspace_size(T, V, code, arr, ns, ctypes.byref(n)), "pstat_workspace_size")
+    return int(n.value)
+
+
+def new_error_flag(device) -> torch.Tensor:
+    """A device int for the kernels' error bits (PSTAT_DEV_*)."""
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def forward(logits: torch.Tensor, labels: torch.Tensor | None, ignore_index: int = -100,
+            shard_bounds=None, *, out=None, workspace=None, dev_error=None):
+    """Per-token logprob, entropy and row statistics (M, ln S).
+
+    Returns (logprob [T] f32, entropy [T] f32, rowstats [T, 2] f32).  `out`
+    may supply the three tensors; `workspace` a uint8 CUDA tensor of at least
+    ``workspace_size`` bytes.
+    """
+    T, V, ld = _rows(logits)
+    dev = logits.device
+    lab = _labels(labels, T, dev)
+    if out is None:
+        lp = torch.empty(T, dtype=torch.float32, device=dev)
+        ent = torch.empty(T, dtype=torch.float32, device=dev)
+        rs = torch.empty(T, 2, dtype=torch.float32, device=dev)
+    else:
+        lp, ent, rs = out
+    arr, ns = _bounds(shard_bounds, V)
+    need = workspace_size(T, V, logits.dtype, shard_bounds)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    _check(_lib.pstat_forward(_ptr(logits), _dtype_code(logits), T, V, ld, _ptr(lab),
+                              int(ignore_index), arr, ns, _ptr(lp), _ptr(ent), _ptr(rs),
+                              _ptr(workspace), workspace.numel(), _ptr(dev_error), _stream(dev)),
+           "pstat_forward")
+    return lp, ent, rs
+
+
+def backward(logits: torch.Tensor, labels: torch.Tensor | None, weights: torch.Tensor | None,
+             rowstats: torch.Tensor | None, ignore_index: int = -100, shard_bounds=None,
+             out_dtype: torch.dtype | None = None, *, out=None, workspace=None, dev_error=None):
+    """dlogits = w (onehot(y) - softmax(z)) as a [T, V] tensor of `out_dtype`
+    (default: the logits dtype)."""
+    T, V, ld = _rows(logits)
+    dev = logits.device
+    lab = _labels(labels, T, dev)
+    out_dtype = out_dtype or logits.dtype
+    if out is None:
+        out = torch.empty(T, V, dtype=out_dtype, device=dev)
+    if out.dim() != 2 or out.shape != (T, V) or out.stride(1) != 1:
+        raise ValueError("out must be [T, V] with contiguous rows")
+    ld_out = out.stride(0) if T > 1 else V
+    w = None if weights is None else weights.contiguous()
+    if w is not None and (w.dtype != torch.float32 or w.shape != (T,)):
+        raise ValueError("weights must be float32 [T]")
+    arr, ns = _bounds(shard_bounds, V)
+    ws_ptr, ws_n = None, 0
+    if rowstats is None:
+        need = workspace_size(T, V, logits.dtype, shard_bounds)
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        ws_ptr, ws_n = _ptr(workspace), workspace.numel()
+    _check(_lib.pstat_backward(_ptr(logits), _dtype_code(logits), T, V, ld, _ptr(lab),
+                               int(ignore_index), _ptr(w), _ptr(rowstats), arr, ns, _ptr(out),
+                               _dtype_code(out), ld_out, ws_ptr, ws_n, _ptr(dev_error),
+                               _stream(dev)),
+           "pstat_backward")
+    return out
+
+
+def lmhead_workspace_size(T: int, V: int, d: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_lib.pstat_lmhead_workspace_size(T, V, d, ctypes.byref(n)), "pstat_lmhead_workspace_size")
+    return int(n.value)
+
+
+def _lmhead_args(hidden, W):
+    if hidden.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
+        raise TypeError("hidden and W must be bfloat16")
+    if not (hidden.is_cuda and W.is_cuda):
+        raise ValueError("hidden and W must be CUDA tensors")
+    hidden, W = hidden.contiguous(), W.contiguous()
+    T, d = hidden.shape
+    V, d2 = W.shape
+    if d != d2:
+        raise ValueError("hidden [T, d] and W [V, d] disagree on d")
+    return hidden, W, T, V, d
+
+
+def lmhead_forward(hidden, W, labels, ignore_index: int = -100, *, workspace=None,
+                   dev_error=None):
+    """Fused lm_head statistics: logits = hidden W^T never leave the chip."""
+    hidden, W, T, V, d = _lmhead_args(hidden, W)
+    dev = hidden.device
+    lab = _labels(labels, T, dev)
+    lp = torch.empty(T, dtype=torch.float32, device=dev)
+    ent = torch.empty(T, dtype=torch.float32, device=dev)
+    rs = torch.empty(T, 2, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(lmhead_workspace_size(T, V, d), 16), dtype=torch.uint8,
+                                device=dev)
+    _check(_lib.pstat_lmhead_fused(_ptr(hidden), _ptr(W), T, V, d, _ptr(lab), int(ignore_index),
+                                   _ptr(lp), _ptr(ent), _ptr(rs), _ptr(workspace),
+                                   workspace.numel(), _ptr(dev_error), _stream(dev)),
+           "pstat_lmhead_fused")
+    return lp, ent, rs
+
+
+def lmhead_backward(hidden, W, labels, weights, rowstats, ignore_index: int = -100, *,
+                    dhidden=None, dW=None, workspace=None, dev_error=None):
+    """Accumulates dhidden += g W and dW += g^T hidden (fp32), g = w (onehot - p)."""
+    hidden, W, T, V, d = _lmhead_args(hidden, W)
+    dev = hidden.device
+    lab = _labels(labels, T, dev)
+    if dhidden is None:
+        dhidden = torch.zeros(T, d, dtype=torch.float32, device=dev)
+    if dW is None:
+        dW = torch.zeros(V, d, dtype=torch.float32, device=dev)
+    w = None if weights is None else weights.contiguous()
+    if workspace is None:
+        workspace = torch.empty(max(lmhead_workspace_size(T, V, d), 16), dtype=torch.uint8,
+                                device=dev)
+    _check(_lib.pstat_lmhead_backward(_ptr(hidden), _ptr(W), T, V, d, _ptr(lab),
+                                      int(ignore_index), _ptr(w), _ptr(rowstats), _ptr(dhidden),
+                                      _ptr(dW), _ptr(workspace), workspace.numel(),
+                                      _ptr(dev_error), _stream(dev)),
+           "pstat_lmhead_backward")
+    return dhidden, dW
+
+
+class PolicyStats(torch.autograd.Function):
+    """logprob (differentiable) and entropy (a no-grad metric) of every row.
+
+    Backward folds the incoming logprob gradient into the per-token weights:
+    dlogits = grad_logprob_t (onehot(y_t) - softmax(z_t)).
+    """
+
+    @staticmethod
+    def forward(ctx, logits, labels, ignore_index=-100, shard_bounds=None):
+        lp, ent, rs = forward(logits, labels, ignore_index, shard_bounds)
+        ctx.save_for_backward(logits, labels, rs)
+        ctx.ignore_index = ignore_index
+        ctx.mark_non_differentiable(ent)
+        return lp, ent
+
+    @staticmethod
+    def backward(ctx, grad_lp, grad_ent):
+        logits, labels, rs = ctx.saved_tensors
+        g = backward(logits, labels, grad_lp.float().contiguous(), rs, ctx.ignore_index)
+        return g, None, None, None
+
+
+def policy_stats(logits, labels, ignore_index: int = -100, shard_bounds=None):
+    """Differentiable (logprob, entropy) through the CUDA kernels."""
+    return PolicyStats.apply(logits, labels, ignore_index, shard_bounds)
