@@ -60,6 +60,28 @@ def dist_env():
     return rank, world, local
 
 
+def rank_seed(base: int, rank: int) -> int:
+    """Each rank draws its own batch of the workload (independent rows)."""
+    return base + 1000 * rank
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """The slowest rank's value (MAX all-reduce); identity on one process."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, steps: int, world: int, ms: float) -> float:
+    """Units processed by all ranks per second, timed by the slowest rank."""
+    return world * units_per_rank * steps / (ms / 1e3)
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -215,7 +237,7 @@ def main():
     from vocab_wide_token_gb300 import inputs, pstat
 
     T = args.tokens
-    d = inputs.fwdbwd_workload(2 + 1000 * rank, dev, T=T)
+    d = inputs.fwdbwd_workload(rank_seed(2, rank), dev, T=T)
     z, y, w = d["logits"], d["labels"], d["weights"]
     err = pstat.new_error_flag(dev)
     lp = torch.empty(T, dtype=torch.float32, device=dev)
@@ -265,13 +287,10 @@ def main():
     ms = start.elapsed_time(end)
     fwd_ms = sum(ev[k][0].elapsed_time(ev[k][1]) for k in range(K)) / K
     bwd_ms = sum(ev[k][1].elapsed_time(ev[k][2]) for k in range(K)) / K
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
     assert err.item() == 0, f"device error bits {err.item()}"
     ms_step = ms / K
-    tok_s = world * T * K / (ms / 1e3)
+    tok_s = whole_job_rate(T, K, world, ms)
 
     # algorithmic bytes (reads of rows whose gradient is identically zero are
     # not needed: ignored rows and zero weights write +0.0 without reading)
@@ -339,12 +358,8 @@ def main():
             e2e_step()
         e2.record(stream)
         barrier()
-        ms2 = s2.elapsed_time(e2)
-        if world > 1:
-            t = torch.tensor([ms2], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ms2 = float(t.item())
-        line["e2e"] = {"value": world * T * Ke / (ms2 / 1e3), "unit": "tokens/s",
+        ms2 = max_over_ranks(s2.elapsed_time(e2), dev)
+        line["e2e"] = {"value": whole_job_rate(T, Ke, world, ms2), "unit": "tokens/s",
                        "h2d_bytes_per_step": zh.numel() * 2 + yh.numel() * 8 + wh.numel() * 4,
                        "d2h_bytes_per_step": outh.numel() * 4, "steps": Ke}
         del zh, zd
