@@ -131,6 +131,39 @@ PSTAT_API int pstat_forward(const void* logits, pstat_dtype dt, int64_t T, int64
                   int n_shards, float* out_logprob, float* out_entropy, float* out_rowstats,
                   void* workspace, size_t ws_bytes, int* dev_error, pstat_stream_t stream);
 
+/* Bytes of the fixed device scratch used by pstat_forward_noalloc (8 MiB). */
+#define PSTAT_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * pstat_forward for callers that cannot allocate device memory.  The pages
+ * have no counterpart to this entry point; it exists for this library's
+ * users.  Some callers must not call cudaMalloc where they compute these
+ * statistics: allocation synchronises the device, a host runtime or
+ * framework may own all device memory through its own pool, or a plain C
+ * caller may have no allocator at all.  This variant takes no workspace and
+ * allocates nothing: its per-chunk scratch is a fixed array of
+ * PSTAT_NOALLOC_SCRATCH_BYTES inside the library, present on every GPU that
+ * loads the library until the process exits.  The caller still passes the
+ * inputs and outputs, with the same meaning, layout and results as
+ * pstat_forward.
+ *   Limit: T * n_chunks * 16 bytes must fit the scratch (n_chunks as in
+ *   pstat_workspace_size; e.g. T <= 13,797 rows at V = 151,936 in bf16),
+ *   else PSTAT_ERR_WORKSPACE is returned before anything is launched.
+ *   The first call on each device looks up the scratch's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ *   Every call on a device shares the one scratch array, which keeps the last
+ *   call's contents.  Nothing in it needs clearing (each call writes every
+ *   record it reads), but calls whose kernels overlap on the GPU (different
+ *   streams, or host threads issuing concurrently) race on it: serialise
+ *   them, e.g. on one stream.
+ */
+PSTAT_API int pstat_forward_noalloc(const void* logits, pstat_dtype dt, int64_t T, int64_t V,
+                                    int64_t ld, const int64_t* labels, int64_t ignore_index,
+                                    const int64_t* shard_bounds, int n_shards, float* out_logprob,
+                                    float* out_entropy, float* out_rowstats, int* dev_error,
+                                    pstat_stream_t stream);
+
 /*
  * Weighted backward dlogits = w (onehot(y) - softmax(z)) (fused elementwise
  * kernel).

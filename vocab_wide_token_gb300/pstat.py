@@ -34,6 +34,9 @@ _lib.pstat_workspace_size.restype = _i32
 _lib.pstat_forward.argtypes = [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _i32, _vp, _vp, _vp,
                                _vp, _sz, _vp, _vp]
 _lib.pstat_forward.restype = _i32
+_lib.pstat_forward_noalloc.argtypes = [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _i32, _vp,
+                                       _vp, _vp, _vp, _vp]
+_lib.pstat_forward_noalloc.restype = _i32
 _lib.pstat_backward.argtypes = [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _vp,
                                 _i32, _i64, _vp, _sz, _vp, _vp]
 _lib.pstat_backward.restype = _i32
@@ -158,6 +161,33 @@ def forward(logits: torch.Tensor, labels: torch.Tensor | None, ignore_index: int
                               int(ignore_index), arr, ns, _ptr(lp), _ptr(ent), _ptr(rs),
                               _ptr(workspace), workspace.numel(), _ptr(dev_error), _stream(dev)),
            "pstat_forward")
+    return lp, ent, rs
+
+
+NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def forward_noalloc(logits: torch.Tensor, labels: torch.Tensor | None, ignore_index: int = -100,
+                    shard_bounds=None, *, out=None, dev_error=None):
+    """Like ``forward`` but through ``pstat_forward_noalloc``: no workspace is
+    passed and the library allocates nothing; its scratch is a fixed
+    8 MiB array inside libpstat.so (T * n_chunks * 16 bytes must fit).  For
+    callers that may not allocate device memory at this point.  Calls that
+    overlap on the GPU share that scratch and race; keep them on one stream."""
+    T, V, ld = _rows(logits)
+    dev = logits.device
+    lab = _labels(labels, T, dev)
+    if out is None:
+        lp = torch.empty(T, dtype=torch.float32, device=dev)
+        ent = torch.empty(T, dtype=torch.float32, device=dev)
+        rs = torch.empty(T, 2, dtype=torch.float32, device=dev)
+    else:
+        lp, ent, rs = out
+    arr, ns = _bounds(shard_bounds, V)
+    _check(_lib.pstat_forward_noalloc(_ptr(logits), _dtype_code(logits), T, V, ld, _ptr(lab),
+                                      int(ignore_index), arr, ns, _ptr(lp), _ptr(ent), _ptr(rs),
+                                      _ptr(dev_error), _stream(dev)),
+           "pstat_forward_noalloc")
     return lp, ent, rs
 
 
