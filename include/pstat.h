@@ -90,6 +90,7 @@ enum {
 #define PSTAT_DEV_BAD_LABEL 0x1 /* label outside [0, V) and != ignore_index */
 #define PSTAT_DEV_EMPTY_ROW 0x2 /* every logit of a row is -inf: softmax undefined */
 #define PSTAT_DEV_TIMEOUT 0x4   /* a bounded wait on an asynchronous copy gave up */
+#define PSTAT_DEV_RANGE 0x8     /* lm_head backward: a value exceeds the fp16 range (65504) */
 
 #define PSTAT_MAX_SHARDS 64
 #define PSTAT_CHUNK_BF16 4096 /* chunk length in elements for bf16 logits */

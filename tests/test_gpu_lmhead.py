@@ -85,3 +85,84 @@ def test_lmhead_full_config_sampled(cuda_lib):
         lp1, ent1, _ = cuda_lib.lmhead_forward(h[r:r + 1], W, y[r:r + 1], IGN)
         assert torch.equal(lp1.view(torch.int32), lp[r:r + 1].view(torch.int32)), r
         assert torch.equal(ent1.view(torch.int32), ent[r:r + 1].view(torch.int32)), r
+
+
+def _frob_rel(a, ref):
+    a = np.asarray(a, np.float64)
+    return float(np.linalg.norm(a - ref) / max(np.linalg.norm(ref), 1e-300))
+
+
+@pytest.mark.parametrize("T,V,d", [(200, 5000, 256), (128, 4096, 64), (1, 300, 128),
+                                   (333, 12345, 512)])
+def test_lmhead_backward_small(cuda_lib, T, V, d):
+    """dhidden += g W and dW += g^T hidden against float64 numpy; Frobenius-
+    relative <= 1e-3 per tensor; a second call accumulates."""
+    h, W, y = _draw(T, V, d, 0.1, 3 * T + V + d)
+    g = torch.Generator(device="cuda").manual_seed(T + d)
+    w = torch.randn(T, generator=g, device="cuda")
+    if T > 3:
+        y[1] = IGN
+        w[2] = 0.0
+    err = cuda_lib.new_error_flag(h.device)
+    lp, ent, rs = cuda_lib.lmhead_forward(h, W, y, IGN, dev_error=err)
+    dh, dW = cuda_lib.lmhead_backward(h, W, y, w, rs, IGN, dev_error=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    rdh, rdW = olm.backward(to_oracle(h), to_oracle(W), y.cpu().numpy(), w.double().cpu().numpy(), IGN)
+    e1 = _frob_rel(dh.double().cpu().numpy(), rdh)
+    e2 = _frob_rel(dW.double().cpu().numpy(), rdW)
+    assert e1 <= 1e-3 and e2 <= 1e-3, (e1, e2)
+    # accumulation: a second call adds the same gradient again
+    cuda_lib.lmhead_backward(h, W, y, w, rs, IGN, dhidden=dh, dW=dW)
+    torch.cuda.synchronize()
+    assert _frob_rel(dh.double().cpu().numpy(), 2 * rdh) <= 1e-3
+    assert _frob_rel(dW.double().cpu().numpy(), 2 * rdW) <= 1e-3
+
+
+def test_lmhead_backward_full_vocab(cuda_lib):
+    """T = 256 tokens against the full vocabulary and hidden size (V = 151936,
+    d = 4096): every element of dhidden and dW through the float64 oracle."""
+    from vocab_wide_token_gb300 import inputs
+
+    d = inputs.lmhead_workload(5, "cuda", T=256)
+    h, W, y, w = d["hidden"], d["W"], d["labels"], d["weights"]
+    y[3] = IGN
+    lp, ent, rs = cuda_lib.lmhead_forward(h, W, y, IGN)
+    dh, dW = cuda_lib.lmhead_backward(h, W, y, w, rs, IGN)
+    torch.cuda.synchronize()
+    rdh, rdW = olm.backward(to_oracle(h), to_oracle(W), y.cpu().numpy(), w.double().cpu().numpy(), IGN)
+    e1 = _frob_rel(dh.double().cpu().numpy(), rdh)
+    e2 = _frob_rel(dW.double().cpu().numpy(), rdW)
+    assert e1 <= 1e-3 and e2 <= 1e-3, (e1, e2)
+
+
+def test_lmhead_backward_full_config(cuda_lib):
+    """hidden [16384, 4096] x W [151936, 4096]: sampled dhidden rows through the
+    oracle, and on every vocabulary row the identity sum_v dW[v] = 0 (each
+    token's gradient sums to zero over the vocabulary)."""
+    from vocab_wide_token_gb300 import inputs
+
+    d = inputs.lmhead_workload(4, "cuda")
+    h, W, y, w = d["hidden"], d["W"], d["labels"], d["weights"]
+    err = cuda_lib.new_error_flag(h.device)
+    lp, ent, rs = cuda_lib.lmhead_forward(h, W, y, IGN, dev_error=err)
+    dh, dW = cuda_lib.lmhead_backward(h, W, y, w, rs, IGN, dev_error=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert torch.isfinite(dh).all() and torch.isfinite(dW).all()
+    rng = np.random.default_rng(9)
+    T = h.shape[0]
+    rows = np.unique(np.concatenate([[0, T - 1], rng.choice(T, 30, replace=False)]))
+    z = olm.logits(to_oracle(h), to_oracle(W), rows)
+    gref = oracle.backward(z, y[rows].cpu().numpy(), w[rows].double().cpu().numpy(), IGN)
+    Wf = oracle.bf16_to_f64(to_oracle(W))
+    rdh = gref @ Wf
+    e1 = _frob_rel(dh[rows].double().cpu().numpy(), rdh)
+    assert e1 <= 1e-3, e1
+    # sum_v g[t, v] = 0 exactly; the fp16 gradient operand leaves at most
+    # 2^-11 sum_v |g[t, v]| <= 2^-10 |w_t| per token, hence the bound below
+    # (plus fp32 accumulation slack).
+    colsum = dW.double().sum(dim=0)
+    bound = 2.0**-10 * (w.double().abs()[:, None] * h.double().abs()).sum(dim=0)
+    scale = dW.double().abs().sum(dim=0)
+    assert torch.all(colsum.abs() <= bound + 1e-4 * scale + 1e-6)

@@ -1,24 +1,41 @@
-// lmhead.cu -- fused lm_head statistics on the 5th-generation tensor cores.
+// lmhead.cu -- fused lm_head on the 5th-generation tensor cores.
 //
-// Logits z = hidden W^T are produced tile by tile (128 tokens x 256 vocab
-// rows, K = d in steps of 64) by tcgen05.mma into tensor memory and folded
-// straight into the per-(token, 4096-column chunk) statistics (m, s, u) that
-// the unfused path also produces; the logits never reach global memory.  The
-// fixed-order combine kernel then turns the chunk statistics into logprob,
-// entropy and (M, ln S).  The chunked lm_head follows TRL PR #6949
-// ("ZeroSyncGRPOTrainer": the vocabulary projection is multiplied chunk by
-// chunk; GEMMs in bf16 with fp32 accumulation).
+// Forward: logits z = hidden W^T are produced tile by tile (128 tokens x 256
+// vocabulary rows, K = d in steps of 64) by tcgen05.mma into tensor memory
+// and folded straight into the per-(token, 4096-column chunk) statistics
+// (m, s, u) that the unfused path also produces; the logits never reach
+// global memory.  The fixed-order combine kernel then gives logprob, entropy
+// and (M, ln S).
 //
-// CTA roles (192 threads, one CTA per SM):
-//   warp 0     TMA producer: 2-D tiled loads of hidden and W k-blocks into a
-//              4-stage shared-memory ring (128-byte swizzle)
+// Backward, per 4096-column vocabulary chunk c (the chunked lm_head of TRL PR
+// #6949 "ZeroSyncGRPOTrainer": GEMMs in a 16-bit dtype, accumulation in fp32
+// buffers):
+//   1. recompute the chunk's logits tile by tile and turn them on chip into
+//      g = w (onehot(y) - e^(z - M - ln S)), stored as fp16 twice: G [T, Vc]
+//      and its transpose Gt [Vc, T];
+//   2. dhidden += G W_c        (A = G, B = W_c^T, both K-major fp16);
+//   3. dW[c]   += Gt hidden    (A = Gt, B = hidden^T, both K-major fp16).
+// fp16 (11-bit significand) keeps the gradient operand within ~3e-4 relative
+// where bf16 would give ~2e-3; hidden and W convert to fp16 exactly while
+// 2^-14 <= |x| <= 65504 (values above flag PSTAT_DEV_RANGE).
+//
+// One warp-specialised persistent GEMM kernel serves every step (192
+// threads, one CTA per SM):
+//   warp 0     TMA producer: 2-D tiled loads of A (128 x 64) and B (256 x 64)
+//              k-blocks into a 4-stage shared-memory ring (128-byte swizzle)
 //   warp 1     allocates 512 TMEM columns (two 128 x 256 fp32 accumulators)
-//              and issues the MMAs from one thread
-//   warps 2-5  epilogue: one thread per token row reads its accumulator row
-//              from TMEM and folds it into the chunk statistics
+//              and issues tcgen05.mma (M=128, N=256, K=16) from one thread
+//   warps 2-5  epilogue: one thread per output row reads its accumulator row
+//              from TMEM (tcgen05.ld.32x32b) and hands it to the epilogue
+//              policy (statistics, gradient tile, or fp32 accumulation)
+// Work is split into units of consecutive N tiles that one CTA processes in
+// order (16 tiles = one statistics chunk in the forward, 1 elsewhere); units
+// are ordered in groups of 32 M tiles so the A slice they share stays in L2.
+// There is no split-K: each output element is a fixed-order K reduction.
 // All waits are bounded; a timeout sets PSTAT_DEV_TIMEOUT and the CTA winds
 // down, draining its copies and MMAs before freeing tensor memory.
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -31,16 +48,16 @@
 #include "tcgen05.cuh"
 
 namespace pstat {
-
 namespace lm {
 
-constexpr int BM = 128;            // tokens per tile (MMA M, TMEM lanes)
-constexpr int BN = 256;            // vocabulary rows per tile (MMA N)
-constexpr int BK = 64;             // K per stage: 64 bf16 = one 128-byte swizzle row
+constexpr int BM = 128;            // output rows per tile (MMA M, TMEM lanes)
+constexpr int BN = 256;            // output columns per tile (MMA N)
+constexpr int BK = 64;             // K per stage: 64 x 16-bit = one 128-byte swizzle row
 constexpr int UK = 16;             // K per tcgen05.mma of kind::f16
 constexpr int STAGES = 4;
-constexpr int TILES_PER_CHUNK = PSTAT_CHUNK_BF16 / BN;  // 16
-constexpr int M_GROUP = 32;        // m-tiles sharing the L2-resident slice of hidden
+constexpr int STATS_TILES = PSTAT_CHUNK_BF16 / BN;  // 16 tiles per statistics chunk
+constexpr int VC = PSTAT_CHUNK_BF16;                // backward vocabulary chunk (columns)
+constexpr int M_GROUP = 32;        // M tiles sharing the L2-resident slice of A
 constexpr int THREADS = 192;
 constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
 constexpr uint32_t B_BYTES = BN * BK * 2;   // 32 KB
@@ -60,59 +77,299 @@ struct Smem {
 };
 constexpr size_t SMEM_BYTES = Smem::total + 1024;  // + alignment slack
 
-struct Geometry {
-    int64_t T, V;
-    int d;
-    int m_tiles, n_tiles, n_chunks, k_blocks;
-    int64_t n_units;
+struct GemmGeo {
+    int m_tiles, n_tiles, k_blocks;
+    int tiles_per_unit;   // consecutive N tiles one CTA processes in order
+    int units_per_m;      // ceil(n_tiles / tiles_per_unit)
+    int64_t n_units;      // m_tiles * units_per_m
+    int b_row0;           // first B row (tensor-map coordinate) of N tile 0
 };
 
-__host__ __device__ inline void unit_coords(const Geometry& g, int64_t u, int& m, int& c) {
-    const int64_t per_group = (int64_t)M_GROUP * g.n_chunks;
+__host__ __device__ inline void unit_coords(const GemmGeo& g, int64_t u, int& m, int& un) {
+    const int64_t per_group = (int64_t)M_GROUP * g.units_per_m;
     const int grp = (int)(u / per_group);
     const int64_t rem = u - (int64_t)grp * per_group;
     int mg = g.m_tiles - grp * M_GROUP;
     if (mg > M_GROUP) mg = M_GROUP;
-    c = (int)(rem / mg);
+    un = (int)(rem / mg);
     m = grp * M_GROUP + (int)(rem % mg);
 }
 
-__device__ __forceinline__ int tiles_in_chunk(const Geometry& g, int c) {
-    const int nt = g.n_tiles - c * TILES_PER_CHUNK;
-    return nt < TILES_PER_CHUNK ? nt : TILES_PER_CHUNK;
+__device__ __forceinline__ int unit_tiles(const GemmGeo& g, int un) {
+    const int nt = g.n_tiles - un * g.tiles_per_unit;
+    return nt < g.tiles_per_unit ? nt : g.tiles_per_unit;
 }
 
-// Folds tile statistics (mj, sj, uj) into the running chunk statistics.
-__device__ __forceinline__ void fold(float& mc, float& sc, float& uc, float mj, float sj, float uj) {
-    if (mj == -INFINITY) return;
-    if (mc == -INFINITY) {
-        mc = mj;
-        sc = sj;
-        uc = uj;
-        return;
-    }
-    if (mj > mc) {
-        const float dm = mc - mj;
-        const float r = expf(dm);
-        uc = r * fmaf(dm, sc, uc);
-        sc = r * sc;
-        mc = mj;
-        sc += sj;
-        uc += uj;
-    } else {
-        const float dm = mj - mc;
-        const float r = expf(dm);
-        sc = fmaf(r, sj, sc);
-        uc = fmaf(r, fmaf(dm, sj, uj), uc);
-    }
+// Instruction descriptor for fp16 operands (A and B both f16, D fp32).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// ---------------------------------------------------------------------------
+// Epilogue policies.  Each has a per-thread State and three hooks called by
+// the epilogue warps: unit_begin, tile (the accumulator of one tile is ready
+// in tensor memory at `taddr`, lane = this thread's output row) and
+// unit_end.
+// ---------------------------------------------------------------------------
+
+// Forward statistics: folds each 256-column tile into running (m, s, u) for
+// its 4096-column chunk and records the target logit.
+struct StatsEpi {
+    int64_t T, V;
+    int n_chunks;
+    const int64_t* labels;
+    int64_t ignore_index;
+    float4* chunk_stats;
+    float* target;
+
+    struct State {
+        int64_t t, y;
+        bool valid;
+        float mc, sc, uc;
+    };
+
+    __device__ void unit_begin(State& st, int m, int /*un*/, int row) const {
+        st.t = (int64_t)m * BM + row;
+        st.valid = st.t < T;
+        st.y = (st.valid && labels) ? labels[st.t] : ignore_index;
+        st.mc = -INFINITY;
+        st.sc = 0.f;
+        st.uc = 0.f;
+    }
+
+    // Folds tile statistics (mj, sj, uj) into the running chunk statistics.
+    __device__ static void fold(State& st, float mj, float sj, float uj) {
+        if (st.mc == -INFINITY) {
+            st.mc = mj;
+            st.sc = sj;
+            st.uc = uj;
+            return;
+        }
+        if (mj > st.mc) {
+            const float dm = st.mc - mj;
+            const float r = expf(dm);
+            st.uc = r * fmaf(dm, st.sc, st.uc) + uj;
+            st.sc = fmaf(r, st.sc, sj);
+            st.mc = mj;
+        } else {
+            const float dm = mj - st.mc;
+            const float r = expf(dm);
+            st.sc = fmaf(r, sj, st.sc);
+            st.uc = fmaf(r, fmaf(dm, sj, uj), st.uc);
+        }
+    }
+
+    __device__ void tile(State& st, uint32_t taddr, int /*m*/, int n, int /*row*/) const {
+        const int64_t col0 = (int64_t)n * BN;
+        const int64_t left = V - col0;
+        const int ncols = left < BN ? (int)left : BN;
+        // pass 1: row maximum over the tile
+        float mx = -INFINITY;
+        for (int p = 0; p < BN / 32; ++p) {
+            if (p * 32 >= ncols) break;
+            float v[32];
+            tmem_ld32(taddr + p * 32, v);
+            tmem_ld_wait();
+            if (p * 32 + 32 <= ncols) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, v[i]);
+            } else {
+                for (int i = 0; i < 32; ++i)
+                    if (p * 32 + i < ncols) mx = fmaxf(mx, v[i]);
+            }
+        }
+        // pass 2: sum e^(z - mx) and sum e^(z - mx)(z - mx), pairs in f32x2
+        const uint64_t negm = f2_pack(-mx, -mx);
+        const uint64_t l2e = f2_pack(kLog2e, kLog2e);
+        uint64_t s2 = 0, u2 = 0;
+        const int64_t yl = st.y - col0;
+        for (int p = 0; p < BN / 32; ++p) {
+            if (p * 32 >= ncols) break;
+            float v[32];
+            tmem_ld32(taddr + p * 32, v);
+            tmem_ld_wait();
+            if (st.valid && yl >= p * 32 && yl < p * 32 + 32 && yl < ncols) {
+                float zy = 0.f;
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (yl == p * 32 + i) zy = v[i];
+                target[st.t] = zy;
+            }
+            if (p * 32 + 32 > ncols) {  // columns past V: e^(-1024) == 0 exactly
+                for (int i = 0; i < 32; ++i)
+                    if (p * 32 + i >= ncols) v[i] = mx - 1024.f;
+            }
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                const uint64_t dd = f2_add(f2_pack(v[i], v[i + 1]), negm);
+                float a0, a1;
+                f2_unpack(f2_mul(dd, l2e), a0, a1);
+                const uint64_t e = f2_pack(ex2_approx(a0), ex2_approx(a1));
+                s2 = f2_add(s2, e);
+                u2 = f2_fma(e, dd, u2);
+            }
+        }
+        float sa, sb, ua, ub;
+        f2_unpack(s2, sa, sb);
+        f2_unpack(u2, ua, ub);
+        fold(st, mx, sa + sb, ua + ub);
+    }
+
+    __device__ void unit_end(State& st, int /*m*/, int un, int /*row*/) const {
+        if (st.valid) chunk_stats[st.t * n_chunks + un] = make_float4(st.mc, st.sc, st.uc, 0.f);
+    }
+};
+
+// Backward step 1: the recomputed logits tile becomes the gradient tile
+// g = w (onehot(y) - e^(z - M - ln S)), written as fp16 to G [rows, ldg]
+// (row-major) and Gt [cols, ldgt] (its transpose).  Rows past T, columns
+// past V, ignored rows and zero-weight rows are written as +0.
+struct GradEpi {
+    int64_t T, V;
+    int64_t c0;            // first vocabulary column of this chunk
+    const int64_t* labels;
+    int64_t ignore_index;
+    const float* weights;
+    const float2* rowstats;
+    __half* G;
+    int64_t ldg;
+    __half* Gt;
+    int64_t ldgt;
+    int* dev_error;
+
+    struct State {
+        int64_t t, y;
+        bool live;
+        float M, log2S, w;
+    };
+
+    __device__ void unit_begin(State& st, int m, int /*un*/, int row) const {
+        st.t = (int64_t)m * BM + row;
+        st.live = false;
+        st.y = ignore_index;
+        st.M = 0.f;
+        st.log2S = 0.f;
+        st.w = 0.f;
+        if (st.t < T) {
+            st.y = labels ? labels[st.t] : ignore_index;
+            st.w = weights ? weights[st.t] : 1.f;
+            if (st.y != ignore_index && st.w != 0.f) {
+                const float2 rs = rowstats[st.t];
+                st.M = rs.x;
+                st.log2S = rs.y * kLog2e;
+                st.live = true;
+                if (st.y < 0 || st.y >= V || !(rs.x > -INFINITY) || !(rs.y == rs.y)) {
+                    st.live = false;  // undefined row: flagged, written as zeros
+                    if (dev_error && c0 == 0)
+                        atomicOr(dev_error, (st.y < 0 || st.y >= V) ? PSTAT_DEV_BAD_LABEL
+                                                                   : PSTAT_DEV_EMPTY_ROW);
+                }
+            }
+        }
+    }
+
+    __device__ void tile(State& st, uint32_t taddr, int /*m*/, int n, int /*row*/) const {
+        const int64_t j0 = (int64_t)n * BN;  // chunk-local column of the tile
+        const uint64_t negM = f2_pack(-st.M, -st.M);
+        const uint64_t l2e = f2_pack(kLog2e, kLog2e);
+        const uint64_t nl2s = f2_pack(-st.log2S, -st.log2S);
+        const float negw = -st.w;
+        bool range = false;
+        for (int p = 0; p < BN / 32; ++p) {
+            const int64_t jp = j0 + p * 32;
+            float v[32];
+            tmem_ld32(taddr + p * 32, v);
+            tmem_ld_wait();
+            float g[32];
+            if (st.live) {
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    const uint64_t d = f2_add(f2_pack(v[i], v[i + 1]), negM);
+                    float a0, a1;
+                    f2_unpack(f2_fma(d, l2e, nl2s), a0, a1);
+                    g[i] = negw * ex2_approx(a0);
+                    g[i + 1] = negw * ex2_approx(a1);
+                }
+                const int64_t yl = st.y - c0 - jp;
+                if (yl >= 0 && yl < 32) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (yl == i) g[i] = st.w + g[i];  // w (1 - p)
+                }
+                const int64_t vcol = c0 + jp;  // vocabulary index of column i is vcol + i
+                if (vcol + 32 > V) {
+                    for (int i = 0; i < 32; ++i)
+                        if (vcol + i >= V) g[i] = 0.f;
+                }
+#pragma unroll
+                for (int i = 0; i < 32; ++i) range |= fabsf(g[i]) > 65504.f;
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) g[i] = 0.f;
+            }
+            // G row segment: 32 fp16 = 4 x 16 bytes
+            uint32_t h2[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const __half2 x = __floats2half2_rn(g[2 * i], g[2 * i + 1]);
+                h2[i] = *reinterpret_cast<const uint32_t*>(&x);
+            }
+            uint4* gp = reinterpret_cast<uint4*>(G + st.t * ldg + jp);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                gp[i] = make_uint4(h2[4 * i], h2[4 * i + 1], h2[4 * i + 2], h2[4 * i + 3]);
+            // Gt column: the 32 lanes of the warp hold 32 consecutive tokens
+            __half* gtp = Gt + jp * ldgt + st.t;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) gtp[(int64_t)i * ldgt] = __float2half_rn(g[i]);
+        }
+        if (range && dev_error) atomicOr(dev_error, PSTAT_DEV_RANGE);
+    }
+
+    __device__ void unit_end(State&, int, int, int) const {}
+};
+
+// Backward steps 2 and 3: out[row0 + r, c] += acc[r, c] for r < rows,
+// c < cols, with 16-byte vector reductions (each element has exactly one
+// writer per launch, so the result does not depend on timing).
+struct AccumEpi {
+    float* out;
+    int64_t ld;
+    int64_t row0;
+    int64_t rows, cols;
+
+    struct State {};
+
+    __device__ void unit_begin(State&, int, int, int) const {}
+
+    __device__ void tile(State&, uint32_t taddr, int m, int n, int row) const {
+        const int64_t r = (int64_t)m * BM + row;
+        const int64_t c0 = (int64_t)n * BN;
+        for (int p = 0; p < BN / 32; ++p) {
+            float v[32];
+            tmem_ld32(taddr + p * 32, v);
+            tmem_ld_wait();
+            if (r >= rows) continue;
+            float* dst = out + (row0 + r) * ld + c0 + p * 32;
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+                if (c0 + p * 32 + i + 4 <= cols)
+                    red_add_v4(dst + i, v[i], v[i + 1], v[i + 2], v[i + 3]);
+            }
+        }
+    }
+
+    __device__ void unit_end(State&, int, int, int) const {}
+};
+
+// ---------------------------------------------------------------------------
+// The GEMM kernel.
+// ---------------------------------------------------------------------------
+template <class Epi, bool kF16>
 __global__ void __launch_bounds__(THREADS, 1)
-    lmhead_stats_kernel(const __grid_constant__ CUtensorMap map_h,
-                        const __grid_constant__ CUtensorMap map_w, const Geometry g,
-                        const int64_t* __restrict__ labels, int64_t ignore_index,
-                        float4* __restrict__ chunk_stats, float* __restrict__ target,
-                        int* __restrict__ dev_error) {
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
+                   const __grid_constant__ CUtensorMap map_b, const GemmGeo g, const Epi epi,
+                   int* __restrict__ dev_error) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -138,8 +395,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         mbar_init(drain, 1);
         fence_mbar_init();
-        prefetch_tensormap(&map_h);
-        prefetch_tensormap(&map_w);
+        prefetch_tensormap(&map_a);
+        prefetch_tensormap(&map_b);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, TMEM_COLS);
@@ -154,15 +411,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
-            const uint64_t pol_h = policy_evict_last();
-            const uint64_t pol_w = policy_evict_first();
+            const uint64_t pol_a = policy_evict_last();
+            const uint64_t pol_b = policy_evict_first();
             uint32_t it = 0;
             for (int64_t u = blockIdx.x; u < g.n_units && !failed; u += gridDim.x) {
-                int m, c;
-                unit_coords(g, u, m, c);
-                const int nt = tiles_in_chunk(g, c);
+                int m, un;
+                unit_coords(g, u, m, un);
+                const int nt = unit_tiles(g, un);
                 for (int j = 0; j < nt && !failed; ++j) {
-                    const int n = c * TILES_PER_CHUNK + j;
+                    const int n = un * g.tiles_per_unit + j;
                     for (int kb = 0; kb < g.k_blocks; ++kb, ++it) {
                         const int s = it % STAGES;
                         const uint32_t ph = (it / STAGES) & 1u;
@@ -171,10 +428,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                             break;
                         }
                         mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-                        tma_load_2d(smem + Smem::a + s * A_BYTES, &map_h, kb * BK, m * BM,
-                                    &full[s], pol_h);
-                        tma_load_2d(smem + Smem::b + s * B_BYTES, &map_w, kb * BK, n * BN,
-                                    &full[s], pol_w);
+                        tma_load_2d(smem + Smem::a + s * A_BYTES, &map_a, kb * BK, m * BM,
+                                    &full[s], pol_a);
+                        tma_load_2d(smem + Smem::b + s * B_BYTES, &map_b, kb * BK,
+                                    g.b_row0 + n * BN, &full[s], pol_b);
                     }
                 }
             }
@@ -182,18 +439,19 @@ __global__ void __launch_bounds__(THREADS, 1)
             // end (on the normal path they all have; after a timeout some may not).
             for (uint32_t k = 0; k < (uint32_t)STAGES && k < it; ++k) {
                 const uint32_t i = it - 1 - k;
-                if (!mbar_wait_bounded(&full[i % STAGES], (i / STAGES) & 1u, WAIT_NS)) failed = true;
+                if (!mbar_wait_bounded(&full[i % STAGES], (i / STAGES) & 1u, WAIT_NS))
+                    failed = true;
             }
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
+            constexpr uint32_t idesc = kF16 ? idesc_f16_f32(BM, BN) : idesc_bf16_f32(BM, BN);
             uint32_t it = 0, tc = 0;
             for (int64_t u = blockIdx.x; u < g.n_units && !failed; u += gridDim.x) {
-                int m, c;
-                unit_coords(g, u, m, c);
-                const int nt = tiles_in_chunk(g, c);
+                int m, un;
+                unit_coords(g, u, m, un);
+                const int nt = unit_tiles(g, un);
                 for (int j = 0; j < nt && !failed; ++j, ++tc) {
                     const uint32_t b = tc & 1u;
                     const uint32_t tph = (tc >> 1) & 1u;
@@ -230,23 +488,18 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!mbar_wait_bounded(drain, 0, WAIT_NS)) failed = true;
         }
     } else {
-        // ---------------- epilogue: statistics ----------------
-        const int q = warp & 3;                 // TMEM lane quadrant of this warp
+        // ---------------- epilogue ----------------
+        const int q = warp & 3;  // TMEM lane quadrant of this warp
         const int row = q * 32 + lane;
-        const uint64_t l2e = f2_pack(kLog2e, kLog2e);
         uint32_t tc = 0;
+        typename Epi::State st;
         for (int64_t u = blockIdx.x; u < g.n_units && !failed; u += gridDim.x) {
-            int m, c;
-            unit_coords(g, u, m, c);
-            const int nt = tiles_in_chunk(g, c);
-            const int64_t t = (int64_t)m * BM + row;
-            const bool valid_t = t < g.T;
-            const int64_t y = (valid_t && labels) ? labels[t] : ignore_index;
-            float mc = -INFINITY, sc = 0.f, uc = 0.f;
+            int m, un;
+            unit_coords(g, u, m, un);
+            const int nt = unit_tiles(g, un);
+            epi.unit_begin(st, m, un, row);
             for (int j = 0; j < nt; ++j, ++tc) {
-                const int64_t col0 = (int64_t)(c * TILES_PER_CHUNK + j) * BN;
-                const int64_t left = g.V - col0;
-                const int ncols = left < BN ? (int)left : BN;
+                const int n = un * g.tiles_per_unit + j;
                 const uint32_t b = tc & 1u;
                 const uint32_t tph = (tc >> 1) & 1u;
                 bool ok = mbar_wait_bounded(&tfull[b], tph, WAIT_NS);
@@ -256,65 +509,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + b * BN;
-                // pass 1: row maximum over the tile
-                float mx = -INFINITY;
-                for (int p = 0; p < BN / 32; ++p) {
-                    if (p * 32 >= ncols) break;
-                    float v[32];
-                    tmem_ld32(taddr + p * 32, v);
-                    tmem_ld_wait();
-                    if (p * 32 + 32 <= ncols) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, v[i]);
-                    } else {
-                        for (int i = 0; i < 32; ++i)
-                            if (p * 32 + i < ncols) mx = fmaxf(mx, v[i]);
-                    }
-                }
-                // pass 2: sum e^(z - mx) and sum e^(z - mx)(z - mx), pairs in f32x2
-                const uint64_t negm = f2_pack(-mx, -mx);
-                uint64_t s2 = 0, u2 = 0;
-                float zy = 0.f;
-                bool have_y = false;
-                const int64_t yl = y - col0;
-                for (int p = 0; p < BN / 32; ++p) {
-                    if (p * 32 >= ncols) break;
-                    float v[32];
-                    tmem_ld32(taddr + p * 32, v);
-                    tmem_ld_wait();
-                    if (yl >= p * 32 && yl < p * 32 + 32 && yl < ncols) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (yl == p * 32 + i) zy = v[i];
-                        have_y = true;
-                    }
-                    if (p * 32 + 32 > ncols) {  // columns past V: e^(-1024) == 0 exactly
-                        for (int i = 0; i < 32; ++i)
-                            if (p * 32 + i >= ncols) v[i] = mx - 1024.f;
-                    }
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        const uint64_t dd = f2_add(f2_pack(v[i], v[i + 1]), negm);
-                        float a0, a1;
-                        f2_unpack(f2_mul(dd, l2e), a0, a1);
-                        const uint64_t e = f2_pack(ex2_approx(a0), ex2_approx(a1));
-                        s2 = f2_add(s2, e);
-                        u2 = f2_fma(e, dd, u2);
-                    }
-                }
+                epi.tile(st, tmem_base + ((uint32_t)(q * 32) << 16) + b * BN, m, n, row);
                 // accumulator b may be overwritten from here on
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tempty[b]);
-                float sa, sb, ua, ub;
-                f2_unpack(s2, sa, sb);
-                f2_unpack(u2, ua, ub);
-                fold(mc, sc, uc, mx, sa + sb, ua + ub);
-                if (have_y && valid_t) target[t] = zy;
             }
             if (failed) break;
-            if (valid_t) chunk_stats[t * g.n_chunks + c] = make_float4(mc, sc, uc, 0.f);
+            epi.unit_end(st, m, un, row);
         }
     }
 
@@ -325,6 +527,37 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, TMEM_COLS);
     }
+}
+
+// ---------------------------------------------------------------------------
+// Transpose with conversion to fp16: dst[c, r] = fp16(src[r, c]) for r < rows,
+// 0 for rows <= r < rows_pad; c < cols.  32 x 32 tiles through shared memory.
+// Values beyond the fp16 range set PSTAT_DEV_RANGE.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256)
+    transpose_bf16_to_f16(const uint16_t* __restrict__ src, int64_t rows, int64_t cols,
+                          int64_t ld_src, __half* __restrict__ dst, int64_t ld_dst,
+                          int64_t rows_pad, int* __restrict__ dev_error) {
+    __shared__ float tile[32][33];
+    const int64_t r0 = (int64_t)blockIdx.y * 32;
+    const int64_t c0 = (int64_t)blockIdx.x * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+    bool range = false;
+#pragma unroll
+    for (int k = 0; k < 32; k += 8) {
+        const int64_t r = r0 + ty + k, c = c0 + tx;
+        float x = 0.f;
+        if (r < rows && c < cols) x = __uint_as_float((uint32_t)src[r * ld_src + c] << 16);
+        range |= fabsf(x) > 65504.f;
+        tile[ty + k][tx] = x;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 32; k += 8) {
+        const int64_t c = c0 + ty + k, r = r0 + tx;
+        if (c < cols && r < rows_pad) dst[c * ld_dst + r] = __float2half_rn(tile[tx][ty + k]);
+    }
+    if (range && dev_error) atomicOr(dev_error, PSTAT_DEV_RANGE);
 }
 
 // ---- host side ------------------------------------------------------------------
@@ -339,57 +572,102 @@ static EncodeTiledFn encode_fn() {
     std::call_once(once, [] {
         void* p = nullptr;
         cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
             fn = reinterpret_cast<EncodeTiledFn>(p);
     });
     return fn;
 }
 
-// Row-major bf16 matrix [rows, cols] -> tensor map with box [box_rows, 64].
-static bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols,
-                     int box_rows) {
+// Row-major 16-bit matrix [rows, cols] (row stride ld elements) -> tensor map
+// with box [box_rows, 64] and the 128-byte swizzle.
+static bool make_map(CUtensorMap* map, bool f16, const void* ptr, int64_t rows, int64_t cols,
+                     int64_t ld, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
     const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+              const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-static Geometry geometry(int64_t T, int64_t V, int64_t d) {
-    Geometry g;
-    g.T = T;
-    g.V = V;
-    g.d = (int)d;
-    g.m_tiles = (int)((T + BM - 1) / BM);
-    g.n_tiles = (int)((V + BN - 1) / BN);
-    g.n_chunks = (int)((V + PSTAT_CHUNK_BF16 - 1) / PSTAT_CHUNK_BF16);
-    g.k_blocks = (int)(d / BK);
-    g.n_units = (int64_t)g.m_tiles * g.n_chunks;
+static GemmGeo geo(int64_t M, int64_t N, int64_t K, int tiles_per_unit, int64_t b_row0) {
+    GemmGeo g;
+    g.m_tiles = (int)((M + BM - 1) / BM);
+    g.n_tiles = (int)((N + BN - 1) / BN);
+    g.k_blocks = (int)((K + BK - 1) / BK);
+    g.tiles_per_unit = tiles_per_unit;
+    g.units_per_m = (g.n_tiles + tiles_per_unit - 1) / tiles_per_unit;
+    g.n_units = (int64_t)g.m_tiles * g.units_per_m;
+    g.b_row0 = (int)b_row0;
     return g;
 }
 
-struct LmWorkspace {
+template <class Epi, bool kF16>
+static cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmGeo& g,
+                               const Epi& epi, int* dev_error, int sm_count, cudaStream_t st) {
+    static std::atomic<bool> configured[64];
+    int devi = 0;
+    cudaGetDevice(&devi);
+    if (devi >= 64 || !configured[devi].load()) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(tc_gemm_kernel<Epi, kF16>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        if (devi < 64) configured[devi].store(true);
+    }
+    if (g.n_units == 0) return cudaSuccess;
+    const int64_t grid = g.n_units < sm_count ? g.n_units : sm_count;
+    tc_gemm_kernel<Epi, kF16><<<(unsigned)grid, THREADS, SMEM_BYTES, st>>>(ma, mb, g, epi,
+                                                                          dev_error);
+    return cudaGetLastError();
+}
+
+static cudaError_t launch_transpose(const uint16_t* src, int64_t rows, int64_t cols,
+                                    int64_t ld_src, __half* dst, int64_t ld_dst, int64_t rows_pad,
+                                    int* dev_error, cudaStream_t st) {
+    const dim3 grid((unsigned)((cols + 31) / 32), (unsigned)((rows_pad + 31) / 32));
+    transpose_bf16_to_f16<<<grid, 256, 0, st>>>(src, rows, cols, ld_src, dst, ld_dst, rows_pad,
+                                                 dev_error);
+    return cudaGetLastError();
+}
+
+// ---- workspace layouts -------------------------------------------------------------
+struct FwdWorkspace {
     size_t stats_off, target_off, total;
 };
-static LmWorkspace lm_layout(int64_t T, int64_t V) {
+static FwdWorkspace fwd_layout(int64_t T, int64_t V) {
     const int64_t nc = (V + PSTAT_CHUNK_BF16 - 1) / PSTAT_CHUNK_BF16;
-    LmWorkspace w;
+    FwdWorkspace w;
     w.stats_off = 0;
     w.target_off = align_up((size_t)T * nc * kChunkRecordBytes, 256);
     w.total = align_up(w.target_off + (size_t)T * sizeof(float), 256);
     return w;
 }
 
+struct BwdWorkspace {
+    int64_t Tp;  // T padded to whole M tiles
+    size_t hT_off, Wt_off, G_off, Gt_off, total;
+};
+static BwdWorkspace bwd_layout(int64_t T, int64_t d) {
+    BwdWorkspace w;
+    w.Tp = (T + BM - 1) / BM * BM;
+    w.hT_off = 0;                                                 // [d, Tp] fp16
+    w.Wt_off = align_up(w.hT_off + (size_t)d * w.Tp * 2, 1024);  // [d, VC] fp16
+    w.G_off = align_up(w.Wt_off + (size_t)d * VC * 2, 1024);     // [Tp, VC] fp16
+    w.Gt_off = align_up(w.G_off + (size_t)w.Tp * VC * 2, 1024);  // [VC, Tp] fp16
+    w.total = align_up(w.Gt_off + (size_t)VC * w.Tp * 2, 1024);
+    return w;
+}
+
 static int check_lm_args(const void* hidden, const void* W, int64_t T, int64_t V, int64_t d) {
     if (T < 0 || V < 1 || d < BK || d % BK != 0 || d > (1 << 20)) return PSTAT_ERR_SHAPE;
-    if (T > (int64_t)INT32_MAX || V > (int64_t)INT32_MAX) return PSTAT_ERR_SHAPE;
+    if (T > (int64_t)INT32_MAX / 2 || V > (int64_t)INT32_MAX / 2) return PSTAT_ERR_SHAPE;
     if (T == 0) return PSTAT_OK;
     if (!hidden || !W) return PSTAT_ERR_NULLPTR;
     if ((reinterpret_cast<uintptr_t>(hidden) & 15u) || (reinterpret_cast<uintptr_t>(W) & 15u))
@@ -407,7 +685,9 @@ extern "C" {
 int pstat_lmhead_workspace_size(int64_t T, int64_t V, int64_t d, size_t* bytes) {
     if (!bytes) return PSTAT_ERR_NULLPTR;
     if (T < 0 || V < 1 || d < lm::BK || d % lm::BK != 0) return PSTAT_ERR_SHAPE;
-    *bytes = lm::lm_layout(T, V).total;
+    const size_t f = lm::fwd_layout(T, V).total;
+    const size_t b = lm::bwd_layout(T, d).total;
+    *bytes = f > b ? f : b;
     return PSTAT_OK;
 }
 
@@ -417,7 +697,7 @@ int pstat_lmhead_fused(const void* hidden, const void* W, int64_t T, int64_t V, 
                        size_t ws_bytes, int* dev_error, pstat_stream_t stream) {
     int rc = lm::check_lm_args(hidden, W, T, V, d);
     if (rc != PSTAT_OK || T == 0) return rc;
-    const lm::LmWorkspace wl = lm::lm_layout(T, V);
+    const lm::FwdWorkspace wl = lm::fwd_layout(T, V);
     if (!workspace || ws_bytes < wl.total) return PSTAT_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) & 15u) return PSTAT_ERR_ALIGN;
     if ((labels && (reinterpret_cast<uintptr_t>(labels) & 7u)) ||
@@ -431,29 +711,26 @@ int pstat_lmhead_fused(const void* hidden, const void* W, int64_t T, int64_t V, 
     if (rc != PSTAT_OK) return rc;
 
     CUtensorMap map_h, map_w;
-    if (!lm::make_map(&map_h, hidden, T, d, lm::BM) || !lm::make_map(&map_w, W, V, d, lm::BN))
+    if (!lm::make_map(&map_h, false, hidden, T, d, d, lm::BM) ||
+        !lm::make_map(&map_w, false, W, V, d, d, lm::BN))
         return PSTAT_ERR_CUDA;
-    const lm::Geometry g = lm::geometry(T, V, d);
     char* ws = static_cast<char*>(workspace);
-    float4* cs = reinterpret_cast<float4*>(ws + wl.stats_off);
-    float* target = reinterpret_cast<float*>(ws + wl.target_off);
+    lm::StatsEpi epi;
+    epi.T = T;
+    epi.V = V;
+    epi.n_chunks = plan.n_chunks;
+    epi.labels = labels;
+    epi.ignore_index = ignore_index;
+    epi.chunk_stats = reinterpret_cast<float4*>(ws + wl.stats_off);
+    epi.target = reinterpret_cast<float*>(ws + wl.target_off);
+    const lm::GemmGeo g = lm::geo(T, V, d, lm::STATS_TILES, 0);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-
-    static std::atomic<bool> configured[64];
-    int devi = 0;
-    cudaGetDevice(&devi);
-    if (devi >= 64 || !configured[devi].load()) {
-        if (cudaFuncSetAttribute(lm::lmhead_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)lm::SMEM_BYTES) != cudaSuccess)
-            return PSTAT_ERR_CUDA;
-        if (devi < 64) configured[devi].store(true);
-    }
-    int64_t grid = g.n_units < dev.sm_count ? g.n_units : dev.sm_count;
-    lm::lmhead_stats_kernel<<<(unsigned)grid, lm::THREADS, lm::SMEM_BYTES, st>>>(
-        map_h, map_w, g, labels, ignore_index, cs, target, dev_error);
-    if (cudaGetLastError() != cudaSuccess) return PSTAT_ERR_CUDA;
-    if (launch_combine(cs, plan, nullptr, PSTAT_BF16, T, V, V, labels, ignore_index, target,
-                       out_logprob, out_entropy, out_rowstats, dev_error, st) != cudaSuccess)
+    if (lm::launch_gemm<lm::StatsEpi, false>(map_h, map_w, g, epi, dev_error, dev.sm_count, st) !=
+        cudaSuccess)
+        return PSTAT_ERR_CUDA;
+    if (launch_combine(epi.chunk_stats, plan, nullptr, PSTAT_BF16, T, V, V, labels, ignore_index,
+                       epi.target, out_logprob, out_entropy, out_rowstats, dev_error,
+                       st) != cudaSuccess)
         return PSTAT_ERR_CUDA;
     return PSTAT_OK;
 }
@@ -462,10 +739,94 @@ int pstat_lmhead_backward(const void* hidden, const void* W, int64_t T, int64_t 
                           const int64_t* labels, int64_t ignore_index, const float* weights,
                           const float* rowstats, float* dhidden, float* dW, void* workspace,
                           size_t ws_bytes, int* dev_error, pstat_stream_t stream) {
-    (void)hidden; (void)W; (void)T; (void)V; (void)d; (void)labels; (void)ignore_index;
-    (void)weights; (void)rowstats; (void)dhidden; (void)dW; (void)workspace; (void)ws_bytes;
-    (void)dev_error; (void)stream;
-    return PSTAT_ERR_UNSUPPORTED;
+    int rc = lm::check_lm_args(hidden, W, T, V, d);
+    if (rc != PSTAT_OK || T == 0) return rc;
+    if (!rowstats || !dhidden || !dW) return PSTAT_ERR_NULLPTR;
+    if ((reinterpret_cast<uintptr_t>(dhidden) & 15u) || (reinterpret_cast<uintptr_t>(dW) & 15u) ||
+        (reinterpret_cast<uintptr_t>(rowstats) & 7u) ||
+        (labels && (reinterpret_cast<uintptr_t>(labels) & 7u)) ||
+        (weights && (reinterpret_cast<uintptr_t>(weights) & 3u)))
+        return PSTAT_ERR_ALIGN;
+    const lm::BwdWorkspace wl = lm::bwd_layout(T, d);
+    if (!workspace || ws_bytes < wl.total) return PSTAT_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 1023u) return PSTAT_ERR_ALIGN;
+    DeviceInfo dev;
+    rc = device_info(&dev);
+    if (rc != PSTAT_OK) return rc;
+
+    char* ws = static_cast<char*>(workspace);
+    __half* hT = reinterpret_cast<__half*>(ws + wl.hT_off);
+    __half* Wt = reinterpret_cast<__half*>(ws + wl.Wt_off);
+    __half* G = reinterpret_cast<__half*>(ws + wl.G_off);
+    __half* Gt = reinterpret_cast<__half*>(ws + wl.Gt_off);
+    const int64_t Tp = wl.Tp;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+    CUtensorMap map_h, map_w, map_G, map_Wt, map_Gt, map_hT;
+    if (!lm::make_map(&map_h, false, hidden, T, d, d, lm::BM) ||
+        !lm::make_map(&map_w, false, W, V, d, d, lm::BN) ||
+        !lm::make_map(&map_G, true, G, Tp, lm::VC, lm::VC, lm::BM) ||
+        !lm::make_map(&map_Wt, true, Wt, d, lm::VC, lm::VC, lm::BN) ||
+        !lm::make_map(&map_Gt, true, Gt, lm::VC, Tp, Tp, lm::BM) ||
+        !lm::make_map(&map_hT, true, hT, d, Tp, Tp, lm::BN))
+        return PSTAT_ERR_CUDA;
+
+    // hidden^T once (fp16, tokens padded to Tp with zeros)
+    if (lm::launch_transpose(static_cast<const uint16_t*>(hidden), T, d, d, hT, Tp, Tp, dev_error,
+                             st) != cudaSuccess)
+        return PSTAT_ERR_CUDA;
+
+    lm::GradEpi ge;
+    ge.T = T;
+    ge.V = V;
+    ge.labels = labels;
+    ge.ignore_index = ignore_index;
+    ge.weights = weights;
+    ge.rowstats = reinterpret_cast<const float2*>(rowstats);
+    ge.G = G;
+    ge.ldg = lm::VC;
+    ge.Gt = Gt;
+    ge.ldgt = Tp;
+    ge.dev_error = dev_error;
+
+    const int64_t n_chunks = (V + lm::VC - 1) / lm::VC;
+    for (int64_t c = 0; c < n_chunks; ++c) {
+        const int64_t c0 = c * lm::VC;
+        const int64_t vc = (V - c0) < lm::VC ? (V - c0) : lm::VC;
+        // W_c^T (fp16; vocabulary columns past the chunk end as zeros)
+        if (lm::launch_transpose(static_cast<const uint16_t*>(W) + c0 * d, vc, d, d, Wt, lm::VC,
+                                 lm::VC, dev_error, st) != cudaSuccess)
+            return PSTAT_ERR_CUDA;
+        // 1. recompute the chunk's logits -> G, Gt
+        ge.c0 = c0;
+        const lm::GemmGeo g1 = lm::geo(Tp, vc, d, 1, c0);
+        if (lm::launch_gemm<lm::GradEpi, false>(map_h, map_w, g1, ge, dev_error, dev.sm_count,
+                                                st) != cudaSuccess)
+            return PSTAT_ERR_CUDA;
+        // 2. dhidden += G W_c
+        lm::AccumEpi e2;
+        e2.out = dhidden;
+        e2.ld = d;
+        e2.row0 = 0;
+        e2.rows = T;
+        e2.cols = d;
+        const lm::GemmGeo g2 = lm::geo(T, d, vc, 1, 0);
+        if (lm::launch_gemm<lm::AccumEpi, true>(map_G, map_Wt, g2, e2, dev_error, dev.sm_count,
+                                                st) != cudaSuccess)
+            return PSTAT_ERR_CUDA;
+        // 3. dW[c0 : c0 + vc] += Gt hidden
+        lm::AccumEpi e3;
+        e3.out = dW;
+        e3.ld = d;
+        e3.row0 = c0;
+        e3.rows = vc;
+        e3.cols = d;
+        const lm::GemmGeo g3 = lm::geo(vc, d, Tp, 1, 0);
+        if (lm::launch_gemm<lm::AccumEpi, true>(map_Gt, map_hT, g3, e3, dev_error, dev.sm_count,
+                                                st) != cudaSuccess)
+            return PSTAT_ERR_CUDA;
+    }
+    return PSTAT_OK;
 }
 
 }  // extern "C"

@@ -129,6 +129,15 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// ---- global reductions -------------------------------------------------------------
+// *p += (a, b, c, d) as one 16-byte vector reduction performed at L2 (p must
+// be 16-byte aligned).
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
+                 "f"(d)
+                 : "memory");
+}
+
 // ---- bf16 helpers -------------------------------------------------------------
 // Element-wise max of two packed bf16 pairs.
 __device__ __forceinline__ uint32_t bf2_max(uint32_t a, uint32_t b) {

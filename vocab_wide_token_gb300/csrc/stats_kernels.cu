@@ -27,21 +27,38 @@ namespace pstat {
 // ---------------------------------------------------------------------------
 // K-A: chunk statistics.
 //
-// Persistent CTAs of kWarps warps.  The flattened list of (row, chunk) items
-// is split into one contiguous range per warp.  Every warp owns a ring of
-// kStages shared-memory slots of 8 KB: its lane 0 streams chunks into the
-// ring with 1-D bulk asynchronous copies (the TMA engine) completing on one
-// mbarrier per slot, kStages - 1 chunks ahead of the one being reduced.
+// Persistent CTAs of kWarps warps, one CTA per SM.  The flattened list of
+// (row, chunk) items is split into one contiguous range per warp.  Every warp
+// owns a ring of kStages shared-memory slots of 8 KB; its lane 0 streams
+// chunks into the ring with 1-D bulk asynchronous copies (the TMA engine)
+// that complete on one mbarrier per slot.  A chunk is read out of its slot
+// once, into registers (lane L holds the 16-byte vectors L, L+32, ..., L+480:
+// 64 registers), and the slot is refilled at once with the chunk kStages
+// ahead, so copies stay in flight while the warp computes.
 // Chunks whose start or byte length is not 16-byte aligned cannot use the
-// bulk copy; the warp loads those element by element into the same slot.
-// Either way the reduction below reads the slot with the same element-to-
-// lane assignment, so the numerics do not depend on alignment or on which
-// warp processes the chunk.
+// bulk copy; the warp loads those element by element into the same slot
+// (padded with -inf to whole vectors).  The reduction sees the same values in
+// the same registers either way, so the numerics do not depend on alignment
+// or on which warp processes the chunk.
+//
+// Per chunk (m = chunk maximum, L = log2(e) rounded to fp32):
+//   m2 = RN(m L), delta = m L - m2 (exact, by one FMA),
+//   a_i = RN(z_i L - m2)      one packed FMA per pair of elements,
+//   e_i = 2^a_i               (MUFU ex2),
+//   s = sum e_i,  u = ln2 * sum e_i a_i.
+// Since a_i = (z_i - m) L + delta up to its own rounding, s and u are the sum
+// of exponentials and the entropy-weighted sum relative to the reference
+// point r = m - delta ln2 (in natural units).  The record is
+// (m, s, u, delta ln2); the combine moves it to any common maximum M with
+// the factor e^((m - M) - delta ln2).  This costs one FMA per element where
+// the direct form z - m, then times log2(e), costs two.
 // ---------------------------------------------------------------------------
-constexpr int kWarps = 8;
-constexpr int kStages = 3;
+constexpr int kWarps = 12;
+constexpr int kStages = 2;
 constexpr int kSlotBytes = 8192;
+constexpr int kVecPerLane = kSlotBytes / 16 / 32;  // 16
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legal copy
+constexpr float kLn2 = 0.6931471805599453f;
 
 static_assert(PSTAT_CHUNK_BF16 * 2 == kSlotBytes, "bf16 chunk must fill one slot");
 static_assert(PSTAT_CHUNK_F32 * 4 == kSlotBytes, "fp32 chunk must fill one slot");
@@ -57,12 +74,19 @@ struct Elem<uint16_t> {  // bf16 bit patterns
     static constexpr int kVec = 8;  // elements per 16-byte vector
     __device__ static uint16_t neg_inf() { return 0xFF80u; }
     __device__ static float to_float(uint16_t v) { return __uint_as_float((uint32_t)v << 16); }
+    __device__ static uint4 neg_inf_vec() {
+        return make_uint4(kBf16NegInf2, kBf16NegInf2, kBf16NegInf2, kBf16NegInf2);
+    }
 };
 template <>
 struct Elem<float> {
     static constexpr int kVec = 4;
     __device__ static float neg_inf() { return -INFINITY; }
     __device__ static float to_float(float v) { return v; }
+    __device__ static uint4 neg_inf_vec() {
+        const uint32_t n = 0xFF800000u;
+        return make_uint4(n, n, n, n);
+    }
 };
 
 // Column span [start, start + len) of chunk g of every row.
@@ -84,76 +108,10 @@ __device__ __forceinline__ uint32_t bf16_round_down(float x) {
 }
 
 // Lower clamp for the exponential pass.  Every element below it has
-// e^(z-m) == 0 in fp32 anyway; clamping keeps z - m finite so that -inf
-// logits add exactly 0 to u instead of 0 * (-inf) = NaN.
+// e^(z-m) == 0 in fp32 anyway; clamping keeps the exponent finite so that
+// -inf logits add exactly 0 to u instead of 0 * (-inf) = NaN.
 __device__ __forceinline__ float clamp_floor(float m) {
     return m - fmaxf(1024.f, fabsf(m) * 0.0625f);
-}
-
-// Warp reduction of the chunk in shared memory (bf16).  Lane L reads the
-// 16-byte vectors L, L+32, L+64, ...; within a lane the four packed pairs
-// accumulate separately and are added in a fixed tree at the end; lanes are
-// combined by an xor butterfly, which gives every lane the same bits.
-__device__ __forceinline__ void chunk_reduce(const uint16_t* buf, int len, int lane, float& m_out,
-                                             float& s_out, float& u_out) {
-    const uint4* v = reinterpret_cast<const uint4*>(buf);
-    const int nvec = (len + 7) >> 3;
-    uint32_t a0 = kBf16NegInf2, a1 = kBf16NegInf2, a2 = kBf16NegInf2, a3 = kBf16NegInf2;
-#pragma unroll 4
-    for (int k = lane; k < nvec; k += 32) {
-        const uint4 q = v[k];
-        a0 = bf2_max(a0, q.x);
-        a1 = bf2_max(a1, q.y);
-        a2 = bf2_max(a2, q.z);
-        a3 = bf2_max(a3, q.w);
-    }
-    const uint32_t a = bf2_max(bf2_max(a0, a1), bf2_max(a2, a3));
-    float m = fmaxf(bf2_lo(a), bf2_hi(a));
-#pragma unroll
-    for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
-    if (m == -INFINITY) {  // every entry masked: contributes nothing
-        m_out = m;
-        s_out = 0.f;
-        u_out = 0.f;
-        return;
-    }
-    const uint32_t f16 = bf16_round_down(clamp_floor(m));
-    const uint32_t fl2 = f16 | (f16 << 16);
-    const uint64_t negm = f2_pack(-m, -m);
-    const uint64_t l2e = f2_pack(kLog2e, kLog2e);
-    uint64_t s0 = 0, s1 = 0, s2 = 0, s3 = 0, u0 = 0, u1 = 0, u2 = 0, u3 = 0;  // (+0, +0) pairs
-    auto step = [&](uint32_t word, uint64_t& s, uint64_t& u) {
-        const uint32_t w = bf2_max(word, fl2);
-        const uint64_t d = f2_add(f2_pack(bf2_lo(w), bf2_hi(w)), negm);
-        float t0, t1;
-        f2_unpack(f2_mul(d, l2e), t0, t1);
-        const uint64_t e = f2_pack(ex2_approx(t0), ex2_approx(t1));
-        s = f2_add(s, e);
-        u = f2_fma(e, d, u);
-    };
-#pragma unroll 2
-    for (int k = lane; k < nvec; k += 32) {
-        const uint4 q = v[k];
-        step(q.x, s0, u0);
-        step(q.y, s1, u1);
-        step(q.z, s2, u2);
-        step(q.w, s3, u3);
-    }
-    auto hsum = [](uint64_t p) {
-        float lo, hi;
-        f2_unpack(p, lo, hi);
-        return lo + hi;
-    };
-    float s = (hsum(s0) + hsum(s1)) + (hsum(s2) + hsum(s3));
-    float u = (hsum(u0) + hsum(u1)) + (hsum(u2) + hsum(u3));
-#pragma unroll
-    for (int off = 16; off; off >>= 1) {
-        s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
-        u += __shfl_xor_sync(0xFFFFFFFFu, u, off);
-    }
-    m_out = m;
-    s_out = s;
-    u_out = u;
 }
 
 __device__ __forceinline__ float max3(float a, float b, float c) {
@@ -162,61 +120,105 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
     return r;
 }
 
-// Warp reduction of the chunk in shared memory (fp32); same scheme with
-// 4-element vectors and two packed accumulator pairs per lane.
-__device__ __forceinline__ void chunk_reduce(const float* buf, int len, int lane, float& m_out,
-                                             float& s_out, float& u_out) {
-    const float4* v = reinterpret_cast<const float4*>(buf);
-    const int nvec = (len + 3) >> 2;
-    float a0 = -INFINITY, a1 = -INFINITY;
-#pragma unroll 4
-    for (int k = lane; k < nvec; k += 32) {
-        const float4 q = v[k];
-        a0 = max3(a0, q.x, q.y);
-        a1 = max3(a1, q.z, q.w);
-    }
-    float m = fmaxf(a0, a1);
+__device__ __forceinline__ float warp_max(float m) {
 #pragma unroll
     for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
-    if (m == -INFINITY) {
-        m_out = m;
-        s_out = 0.f;
-        u_out = 0.f;
-        return;
+    return m;
+}
+
+__device__ __forceinline__ float hsum2(uint64_t p) {
+    float lo, hi;
+    f2_unpack(p, lo, hi);
+    return lo + hi;
+}
+
+// Statistics of one chunk held in registers (bf16).  Lane-local sums run over
+// the lane's vectors in ascending order with one packed accumulator per
+// 32-bit word; the four are added in a fixed tree, then lanes by an xor
+// butterfly (which leaves the same bits in every lane).
+__device__ __forceinline__ float4 reduce_regs(const uint4 (&q)[kVecPerLane], uint16_t*) {
+    uint32_t a0 = q[0].x, a1 = q[0].y, a2 = q[0].z, a3 = q[0].w;
+#pragma unroll
+    for (int j = 1; j < kVecPerLane; ++j) {
+        a0 = bf2_max(a0, q[j].x);
+        a1 = bf2_max(a1, q[j].y);
+        a2 = bf2_max(a2, q[j].z);
+        a3 = bf2_max(a3, q[j].w);
     }
-    const float fl = clamp_floor(m);
-    const uint64_t negm = f2_pack(-m, -m);
-    const uint64_t l2e = f2_pack(kLog2e, kLog2e);
-    uint64_t s0 = 0, s1 = 0, u0 = 0, u1 = 0;
-    auto step = [&](float x, float y, uint64_t& s, uint64_t& u) {
-        const uint64_t d = f2_add(f2_pack(fmaxf(x, fl), fmaxf(y, fl)), negm);
-        float t0, t1;
-        f2_unpack(f2_mul(d, l2e), t0, t1);
-        const uint64_t e = f2_pack(ex2_approx(t0), ex2_approx(t1));
+    const uint32_t a = bf2_max(bf2_max(a0, a1), bf2_max(a2, a3));
+    const float m = warp_max(fmaxf(bf2_lo(a), bf2_hi(a)));
+    if (m == -INFINITY) return make_float4(m, 0.f, 0.f, 0.f);  // fully masked chunk
+    const float m2 = m * kLog2e;
+    const float delta = fmaf(m, kLog2e, -m2);
+    const uint32_t f16 = bf16_round_down(clamp_floor(m));
+    const uint32_t fl2 = f16 | (f16 << 16);
+    const uint64_t L2 = f2_pack(kLog2e, kLog2e);
+    const uint64_t nm2 = f2_pack(-m2, -m2);
+    uint64_t s0 = 0, s1 = 0, s2 = 0, s3 = 0, u0 = 0, u1 = 0, u2 = 0, u3 = 0;  // (+0, +0) pairs
+    auto step = [&](uint32_t word, uint64_t& s, uint64_t& u) {
+        const uint32_t w = bf2_max(word, fl2);
+        const uint64_t a = f2_fma(f2_pack(bf2_lo(w), bf2_hi(w)), L2, nm2);
+        float a0_, a1_;
+        f2_unpack(a, a0_, a1_);
+        const uint64_t e = f2_pack(ex2_approx(a0_), ex2_approx(a1_));
         s = f2_add(s, e);
-        u = f2_fma(e, d, u);
+        u = f2_fma(e, a, u);
     };
-#pragma unroll 2
-    for (int k = lane; k < nvec; k += 32) {
-        const float4 q = v[k];
-        step(q.x, q.y, s0, u0);
-        step(q.z, q.w, s1, u1);
+#pragma unroll
+    for (int j = 0; j < kVecPerLane; ++j) {
+        step(q[j].x, s0, u0);
+        step(q[j].y, s1, u1);
+        step(q[j].z, s2, u2);
+        step(q[j].w, s3, u3);
     }
-    auto hsum = [](uint64_t p) {
-        float lo, hi;
-        f2_unpack(p, lo, hi);
-        return lo + hi;
-    };
-    float s = hsum(s0) + hsum(s1);
-    float u = hsum(u0) + hsum(u1);
+    float s = (hsum2(s0) + hsum2(s1)) + (hsum2(s2) + hsum2(s3));
+    float u = (hsum2(u0) + hsum2(u1)) + (hsum2(u2) + hsum2(u3));
 #pragma unroll
     for (int off = 16; off; off >>= 1) {
         s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
         u += __shfl_xor_sync(0xFFFFFFFFu, u, off);
     }
-    m_out = m;
-    s_out = s;
-    u_out = u;
+    return make_float4(m, s, u * kLn2, delta * kLn2);
+}
+
+// Same for fp32 chunks: 4-element vectors, two packed accumulators per lane.
+__device__ __forceinline__ float4 reduce_regs(const uint4 (&q)[kVecPerLane], float*) {
+    float a0 = -INFINITY, a1 = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kVecPerLane; ++j) {
+        a0 = max3(a0, __uint_as_float(q[j].x), __uint_as_float(q[j].y));
+        a1 = max3(a1, __uint_as_float(q[j].z), __uint_as_float(q[j].w));
+    }
+    const float m = warp_max(fmaxf(a0, a1));
+    if (m == -INFINITY) return make_float4(m, 0.f, 0.f, 0.f);
+    const float m2 = m * kLog2e;
+    const float delta = fmaf(m, kLog2e, -m2);
+    const float fl = clamp_floor(m);
+    const uint64_t L2 = f2_pack(kLog2e, kLog2e);
+    const uint64_t nm2 = f2_pack(-m2, -m2);
+    uint64_t s0 = 0, s1 = 0, u0 = 0, u1 = 0;
+    auto step = [&](uint32_t x, uint32_t y, uint64_t& s, uint64_t& u) {
+        const uint64_t a = f2_fma(f2_pack(fmaxf(__uint_as_float(x), fl), fmaxf(__uint_as_float(y), fl)),
+                                  L2, nm2);
+        float a0_, a1_;
+        f2_unpack(a, a0_, a1_);
+        const uint64_t e = f2_pack(ex2_approx(a0_), ex2_approx(a1_));
+        s = f2_add(s, e);
+        u = f2_fma(e, a, u);
+    };
+#pragma unroll
+    for (int j = 0; j < kVecPerLane; ++j) {
+        step(q[j].x, q[j].y, s0, u0);
+        step(q[j].z, q[j].w, s1, u1);
+    }
+    float s = hsum2(s0) + hsum2(s1);
+    float u = hsum2(u0) + hsum2(u1);
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+        s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
+        u += __shfl_xor_sync(0xFFFFFFFFu, u, off);
+    }
+    return make_float4(m, s, u * kLn2, delta * kLn2);
 }
 
 template <typename E>
@@ -292,12 +294,21 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
             for (int k = lane; k < padded; k += 32) buf[k] = (k < len) ? src[k] : Elem<E>::neg_inf();
             __syncwarp();
         }
-        float m, s, u;
-        chunk_reduce(buf, len, lane, m, s, u);
-        if (lane == 0) out[i0 + j] = make_float4(m, s, u, 0.f);
+        // Slot -> registers; vectors past the chunk end read as -inf.
+        constexpr int kVec = Elem<E>::kVec;
+        const int nvec = (len + kVec - 1) / kVec;
+        const uint4* v = reinterpret_cast<const uint4*>(buf);
+        uint4 q[kVecPerLane];
+#pragma unroll
+        for (int jj = 0; jj < kVecPerLane; ++jj) {
+            const int k = lane + 32 * jj;
+            q[jj] = (k < nvec) ? v[k] : Elem<E>::neg_inf_vec();
+        }
         __syncwarp();
         fence_proxy_async_smem();  // our reads of the slot precede the next bulk write into it
         if (j + kStages < n) issue(i0 + j + kStages, slot);
+        const float4 r = reduce_regs(q, (E*)nullptr);
+        if (lane == 0) out[i0 + j] = r;
     }
     if (timed_out) {
         if (lane == 0 && dev_error) atomicOr(dev_error, PSTAT_DEV_TIMEOUT);
@@ -317,23 +328,21 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 
 // ---------------------------------------------------------------------------
 // K-B: fixed-order combine, one thread per row.
-// Within a shard: M_s = max of its chunk maxima, then its chunks in ascending
-// order are moved to M_s and summed:
-//     S_s = sum_c s_c e^(m_c - M_s),  U_s = sum_c e^(m_c - M_s)(u_c + (m_c - M_s) s_c).
+// A chunk record (m, s, u, dr) holds its sums relative to the reference point
+// m - dr (dr = 0 when the producer shifted by m itself).  Within a shard:
+// M_s = max of its chunk maxima, then its chunks in ascending order are moved
+// to M_s and summed, with f = e^((m_c - M_s) - dr_c):
+//     S_s = sum_c f s_c,   U_s = sum_c f (u_c + ((m_c - M_s) - dr_c) s_c).
 // Across shards: the same with the row maximum M, shards in ascending order.
 // Chunks or shards whose maximum is -inf (fully masked) are skipped.
+// The CTA first copies its rows' records into shared memory with coalesced
+// loads (when they fit), so each thread's sequential fold reads on-chip data.
 // ---------------------------------------------------------------------------
-template <typename E>
-__global__ void __launch_bounds__(128)
-    combine_kernel(const float4* __restrict__ cs, const __grid_constant__ ShardPlan plan,
-                   const E* __restrict__ logits, int64_t T, int64_t V, int64_t ld,
-                   const int64_t* __restrict__ labels, int64_t ignore_index,
-                   const float* __restrict__ target, float* __restrict__ logprob,
-                   float* __restrict__ entropy, float* __restrict__ rowstats,
-                   int* __restrict__ dev_error) {
-    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (t >= T) return;
-    const float4* c = cs + t * plan.n_chunks;
+constexpr int kCombineRows = 32;     // rows per CTA
+constexpr int kCombineThreads = 128;
+constexpr int kCombineSmemRecords = 3072;  // 48 KB of float4
+
+__device__ __forceinline__ float4 fold_row(const float4* c, const ShardPlan& plan) {
     float M = -INFINITY;
     for (int g = 0; g < plan.n_chunks; ++g) M = fmaxf(M, c[g].x);
     float S = 0.f, U = 0.f;
@@ -346,7 +355,7 @@ __global__ void __launch_bounds__(128)
             for (int g = plan.cum[sh]; g < plan.cum[sh + 1]; ++g) {
                 const float4 r = c[g];
                 if (r.x == -INFINITY) continue;
-                const float dm = r.x - Ms;
+                const float dm = (r.x - Ms) - r.w;
                 const float f = expf(dm);
                 Ss = fmaf(r.y, f, Ss);
                 Us = fmaf(f, fmaf(dm, r.y, r.z), Us);
@@ -357,6 +366,32 @@ __global__ void __launch_bounds__(128)
             U = fmaf(f, fmaf(dM, Ss, Us), U);
         }
     }
+    return make_float4(M, S, U, 0.f);
+}
+
+template <typename E>
+__global__ void __launch_bounds__(kCombineThreads)
+    combine_kernel(const float4* __restrict__ cs, const __grid_constant__ ShardPlan plan,
+                   const E* __restrict__ logits, int64_t T, int64_t V, int64_t ld,
+                   const int64_t* __restrict__ labels, int64_t ignore_index,
+                   const float* __restrict__ target, float* __restrict__ logprob,
+                   float* __restrict__ entropy, float* __restrict__ rowstats,
+                   int* __restrict__ dev_error) {
+    __shared__ float4 stage[kCombineSmemRecords];
+    const int64_t t0 = (int64_t)blockIdx.x * kCombineRows;
+    const int64_t rows = min((int64_t)kCombineRows, T - t0);
+    const int nc = plan.n_chunks;
+    const bool staged = (int64_t)kCombineRows * nc <= kCombineSmemRecords;
+    if (staged) {
+        const int64_t n = rows * nc;
+        const float4* src = cs + t0 * nc;
+        for (int64_t i = threadIdx.x; i < n; i += kCombineThreads) stage[i] = src[i];
+        __syncthreads();
+    }
+    if (threadIdx.x >= rows) return;
+    const int64_t t = t0 + threadIdx.x;
+    const float4 st = fold_row(staged ? stage + (int64_t)threadIdx.x * nc : cs + t * nc, plan);
+    const float M = st.x, S = st.y, U = st.z;
     int err = 0;
     float lnS, H, lp;
     if (!(M > -INFINITY)) {
@@ -585,8 +620,8 @@ cudaError_t launch_combine(const float4* cs, const ShardPlan& plan, const void* 
                            const int64_t* labels, int64_t ignore_index, const float* target,
                            float* logprob, float* entropy, float* rowstats, int* dev_error,
                            cudaStream_t stream) {
-    const int threads = 128;
-    const unsigned grid = (unsigned)((T + threads - 1) / threads);
+    const int threads = kCombineThreads;
+    const unsigned grid = (unsigned)((T + kCombineRows - 1) / kCombineRows);
     if (dt == PSTAT_BF16)
         combine_kernel<uint16_t><<<grid, threads, 0, stream>>>(
             cs, plan, static_cast<const uint16_t*>(logits), T, V, ld, labels, ignore_index,
