@@ -1,9 +1,11 @@
 """Benchmark: per-token logprob + entropy + weighted backward at V = 151,936.
 
-One step is one pass of the hot path over one batch: pstat_forward (chunk
-statistics + fixed-order combine) and pstat_backward (fused weighted
-gradient, bf16 dlogits) on T = 8192 rows of bf16 logits N(0, 2^2), labels
-sampled from each row's softmax, weights N(0, 1) x a 0/1 mask with 20% zeros.
+One step is one pass of the hot path over one batch of T = 8192 rows of bf16
+logits N(0, 2^2), labels sampled from each row's softmax, weights N(0, 1) x a
+0/1 mask with 20% zeros: logprob, entropy and bf16 dlogits.  The headline
+step is pstat_forward + pstat_backward (each kernel's bandwidth under
+`kernels`); the same workload through pstat_forward_backward (statistics and
+gradient in one pass over the logits) is timed in the same run under `fused`.
 
 Prints ONE JSON line (rank 0).  `value` is whole-job tokens/s with inputs
 resident in HBM; `e2e` is the same metric through the Python/C-ABI calls with
@@ -50,6 +52,8 @@ def parse():
     p.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
     p.add_argument("--no-lmhead", action="store_true", help="skip the fused lm_head variant")
+    p.add_argument("--lmhead-tokens", type=int, default=16384,
+                   help="tokens of the lm_head variant (profiling: smaller)")
     return p.parse_args()
 
 
@@ -206,16 +210,18 @@ def run_reference(args):
 
 
 def traffic_record(kernel: str):
-    """dram bytes per launch recorded by ncu, if the kernel source is unchanged."""
+    """DRAM bytes per launch that ncu recorded for `kernel` (profiles/
+    ncu_traffic.json), scaled later to this run's rows; None once any source
+    file the record lists has changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
-    src = os.path.join(ROOT, "vocab_wide_token_gb300", "csrc", "stats_kernels.cu")
     try:
         with open(path) as f:
             rec = json.load(f)[kernel]
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-        if rec.get("source_sha256") != sha:
-            return None, None
-        return float(rec["dram_bytes_per_launch"]), float(rec.get("rows", 0))
+        for src, sha in rec["sources"].items():
+            with open(os.path.join(ROOT, src), "rb") as fh:
+                if hashlib.sha256(fh.read()).hexdigest() != sha:
+                    return None, None
+        return float(rec["dram_bytes_per_launch"]), float(rec["rows"])
     except Exception:
         return None, None
 
@@ -247,12 +253,16 @@ def main():
     ws = torch.empty(pstat.workspace_size(T, V, torch.bfloat16), dtype=torch.uint8, device=dev)
     active_rows = int(((w != 0) & (y != -100)).sum().item())
 
-    def step():
+    def two_call():
         pstat.forward(z, y, -100, None, out=(lp, ent, rs), workspace=ws, dev_error=err)
         pstat.backward(z, y, w, rs, -100, out=g, dev_error=err)
 
+    def fused():
+        pstat.forward_backward(z, y, w, -100, out=(lp, ent, rs), dlogits=g, dev_error=err)
+
     for _ in range(max(args.warmup, 3)):
-        step()
+        two_call()
+        fused()
     torch.cuda.synchronize()
 
     def barrier():
@@ -260,7 +270,8 @@ def main():
             torch.distributed.barrier()
         torch.cuda.synchronize()
 
-    # ---- timed region: device-resident inputs -------------------------------
+    # ---- timed regions: device-resident inputs --------------------------------
+    # (a) the two calls, with events around each; (b) the fused single pass.
     stream = torch.cuda.current_stream(dev)
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
@@ -269,62 +280,80 @@ def main():
     time.sleep(0.3)
     barrier()
     t_wall0 = time.time()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
+    start_a = torch.cuda.Event(enable_timing=True)
+    end_a = torch.cuda.Event(enable_timing=True)
+    start_a.record(stream)
     for k in range(K):
         ev[k][0].record(stream)
         pstat.forward(z, y, -100, None, out=(lp, ent, rs), workspace=ws, dev_error=err)
         ev[k][1].record(stream)
         pstat.backward(z, y, w, rs, -100, out=g, dev_error=err)
         ev[k][2].record(stream)
-    end.record(stream)
+    end_a.record(stream)
+    barrier()
+    evb = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    start_b = torch.cuda.Event(enable_timing=True)
+    end_b = torch.cuda.Event(enable_timing=True)
+    start_b.record(stream)
+    for k in range(K):
+        evb[k].record(stream)
+        pstat.forward_backward(z, y, w, -100, out=(lp, ent, rs), dlogits=g, dev_error=err)
+    evb[K].record(stream)
+    end_b.record(stream)
     barrier()
     t_wall1 = time.time()
     clocks.window = (t_wall0, t_wall1)
     time.sleep(0.25)
     clocks.stop()
-    ms = start.elapsed_time(end)
+    ms_a = max_over_ranks(start_a.elapsed_time(end_a), dev)
+    ms_b = max_over_ranks(start_b.elapsed_time(end_b), dev)
     fwd_ms = sum(ev[k][0].elapsed_time(ev[k][1]) for k in range(K)) / K
     bwd_ms = sum(ev[k][1].elapsed_time(ev[k][2]) for k in range(K)) / K
-    ms = max_over_ranks(ms, dev)
+    fused_ms = sum(evb[k].elapsed_time(evb[k + 1]) for k in range(K)) / K
     assert err.item() == 0, f"device error bits {err.item()}"
-    ms_step = ms / K
-    tok_s = whole_job_rate(T, K, world, ms)
 
-    # algorithmic bytes (reads of rows whose gradient is identically zero are
-    # not needed: ignored rows and zero weights write +0.0 without reading)
-    fwd_bytes = T * (2 * V + 8 + 16)                 # logits, label, logprob/entropy/rowstats
-    bwd_bytes = active_rows * 2 * V + T * (2 * V + 20)  # read active rows, write every row
+    # Algorithmic bytes.  Two calls: the forward reads every row; the backward
+    # reads the rows whose gradient is not identically zero (ignored rows and
+    # zero weights are written as +0.0 without reading) and writes every row.
+    # Fused: every row is read once from HBM and written once.
+    fwd_bytes = T * (2 * V + 8 + 16)                    # logits, label, logprob/entropy/rowstats
+    bwd_bytes = active_rows * 2 * V + T * (2 * V + 20)  # reads of active rows, writes, row data
+    fused_bytes = T * (2 * V + 2 * V + 8 + 4 + 16)
     hbm, tflops, tflops_sus, peak_kind = measured_peaks()
     bwd_gbs = bwd_bytes / (bwd_ms / 1e3) / 1e9
     fwd_gbs = fwd_bytes / (fwd_ms / 1e3) / 1e9
-    step_gbs = (fwd_bytes + bwd_bytes) / (ms_step / 1e3) / 1e9
+    fused_gbs = fused_bytes / (fused_ms / 1e3) / 1e9
     dominant = "backward_kernel" if bwd_ms >= fwd_ms else "chunk_stats_kernel"
     traffic, traffic_rows = traffic_record(dominant)
     if traffic is not None and traffic_rows:
         traffic = traffic * T / traffic_rows
-    roof = {"bound": "hbm", "kernel": dominant,
-            "achieved": bwd_gbs if dominant == "backward_kernel" else fwd_gbs,
-            "peak": hbm, "unit": "GB/s", "peak_kind": peak_kind,
-            "traffic": traffic,
-            "algorithmic_bytes_per_launch": bwd_bytes if dominant == "backward_kernel" else fwd_bytes}
-    roof["frac"] = roof["achieved"] / hbm
+    dom_bytes = bwd_bytes if dominant == "backward_kernel" else fwd_bytes
+    dom_gbs = bwd_gbs if dominant == "backward_kernel" else fwd_gbs
+    roof = {"bound": "hbm", "kernel": dominant, "achieved": dom_gbs, "peak": hbm,
+            "unit": "GB/s", "frac": dom_gbs / hbm, "peak_kind": peak_kind, "traffic": traffic,
+            "algorithmic_bytes_per_launch": dom_bytes}
+    ms_step = ms_a / K
+    tok_s = whole_job_rate(T, K, world, ms_a)
 
     line = {
         "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"fwdbwd: T={T} rows per GPU x V={V} bf16 logits N(0,2^2), "
-                               "sampled labels, weights N(0,1) x mask(20% zero), bf16 dlogits",
+                               "sampled labels, weights N(0,1) x mask(20% zero), bf16 dlogits; "
+                               "step = pstat_forward + pstat_backward",
                    "global_batch": T * world, "seq_len": None, "parallelism": f"dp{world}",
                    "l2": "inputs larger than L2 (2.49 GB logits per rank)"},
-        "gbs": step_gbs,
+        "gbs": (fwd_bytes + bwd_bytes) / (ms_step / 1e3) / 1e9,
         "kernels": {"forward_ms": fwd_ms, "forward_gbs": fwd_gbs, "forward_frac": fwd_gbs / hbm,
-                    "backward_ms": bwd_ms, "backward_gbs": bwd_gbs, "backward_frac": bwd_gbs / hbm,
-                    "active_rows": active_rows},
+                    "backward_ms": bwd_ms, "backward_gbs": bwd_gbs,
+                    "backward_frac": bwd_gbs / hbm, "active_rows": active_rows},
         "roofline": roof,
         "gpu_launches": 3 * K,
+        "fused": {"step": "pstat_forward_backward (one pass over the logits)",
+                  "value": whole_job_rate(T, K, world, ms_b), "ms_per_step": ms_b / K,
+                  "kernel_ms": fused_ms, "gbs": fused_gbs, "frac": fused_gbs / hbm,
+                  "algorithmic_bytes_per_launch": fused_bytes, "gpu_launches": K},
         "clocks": clocks.summary(),
     }
 
@@ -366,7 +395,8 @@ def main():
 
     # ---- fused lm_head variant (rank 0 reports) ------------------------------
     if not args.no_lmhead:
-        line["lmhead"] = bench_lmhead(pstat, dev, tflops, tflops_sus, peak_kind)
+        line["lmhead"] = bench_lmhead(pstat, dev, tflops, tflops_sus, peak_kind,
+                                      T=args.lmhead_tokens)
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N=1 only) ------
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -385,9 +415,11 @@ def main():
         torch.distributed.destroy_process_group()
 
 
-def bench_lmhead(pstat, dev, tflops, tflops_sus, peak_kind, steps=5, warmup=2):
-    """Fused lm_head statistics on hidden [16384, 4096] x W [151936, 4096] bf16
-    (the tcgen05 GEMM with the statistics epilogue + the combine kernel)."""
+def bench_lmhead(pstat, dev, tflops, tflops_sus, peak_kind, T=16384, steps=3, warmup=1):
+    """Fused lm_head on hidden [T, 4096] x W [151936, 4096] bf16: the forward
+    (tcgen05 GEMM with the statistics epilogue + combine; 2 T V d flops) and
+    the backward (per 4096-column chunk: recompute GEMM -> fp16 gradient tile,
+    dhidden GEMM, dW GEMM; 6 T V d flops)."""
     import torch
     from vocab_wide_token_gb300 import inputs
 
@@ -395,32 +427,59 @@ def bench_lmhead(pstat, dev, tflops, tflops_sus, peak_kind, steps=5, warmup=2):
         pstat.lmhead_workspace_size(16, V, 4096)
     except pstat.PstatError as e:
         return {"status": f"unavailable: {e}"}
-    d = inputs.lmhead_workload(4, dev)
-    h, W, y = d["hidden"], d["W"], d["labels"]
+    d = inputs.lmhead_workload(4, dev, T=T)
+    h, W, y, w = d["hidden"], d["W"], d["labels"], d["weights"]
     T, dm = h.shape
     err = pstat.new_error_flag(dev)
     ws = torch.empty(pstat.lmhead_workspace_size(T, V, dm), dtype=torch.uint8, device=dev)
-    for _ in range(warmup):
-        pstat.lmhead_forward(h, W, y, -100, workspace=ws, dev_error=err)
-    torch.cuda.synchronize()
+    dh = torch.zeros(T, dm, dtype=torch.float32, device=dev)
+    dW = torch.zeros(V, dm, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        pstat.lmhead_forward(h, W, y, -100, workspace=ws, dev_error=err)
-    b.record(stream)
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / steps
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
+
+    out = {}
+
+    def fwd():
+        out["fwd"] = pstat.lmhead_forward(h, W, y, -100, workspace=ws, dev_error=err)
+
+    fwd_ms = timed(fwd)
+    rs = out["fwd"][2]
+
+    def bwd():
+        pstat.lmhead_backward(h, W, y, w, rs, -100, dhidden=dh, dW=dW, workspace=ws,
+                              dev_error=err)
+
+    bwd_ms = timed(bwd)
     assert err.item() == 0, f"device error bits {err.item()}"
-    flop = 2.0 * T * V * dm
-    achieved = flop / (ms / 1e3) / 1e12
-    return {"status": "ok", "workload": f"hidden [{T}, {dm}] x W [{V}, {dm}] bf16",
-            "forward_ms": ms, "forward_tokens_per_s": T / (ms / 1e3),
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": tflops,
-                         "unit": "TFLOP/s", "frac": achieved / tflops, "peak_kind": peak_kind,
+    flop_f = 2.0 * T * V * dm
+    flop_b = 6.0 * T * V * dm
+    af = flop_f / (fwd_ms / 1e3) / 1e12
+    ab = flop_b / (bwd_ms / 1e3) / 1e12
+    n_chunks = (V + 4095) // 4096
+    return {"status": "ok", "workload": f"hidden [{T}, {dm}] x W [{V}, {dm}] bf16, sampled labels",
+            "forward_ms": fwd_ms, "forward_tokens_per_s": T / (fwd_ms / 1e3),
+            "backward_ms": bwd_ms, "backward_tokens_per_s": T / (bwd_ms / 1e3),
+            "roofline": {"bound": "tensor", "kernel": "tc_gemm_kernel<StatsEpi>",
+                         "achieved": af, "peak": tflops, "unit": "TFLOP/s",
+                         "frac": af / tflops, "peak_kind": f"{peak_kind} burst",
                          "traffic": None},
-            "gpu_launches_per_call": 2}
+            "backward_roofline": {"bound": "tensor", "achieved": ab, "peak": tflops_sus,
+                                  "unit": "TFLOP/s", "frac": ab / tflops_sus,
+                                  "peak_kind": f"{peak_kind} sustained",
+                                  "algorithmic_flop": flop_b},
+            "gpu_launches_per_forward": 2, "gpu_launches_per_backward": 1 + 4 * n_chunks}
 
 
 if __name__ == "__main__":

@@ -184,6 +184,25 @@ PSTAT_API int pstat_backward(const void* logits, pstat_dtype dt, int64_t T, int6
                    size_t ws_bytes, int* dev_error, pstat_stream_t stream);
 
 /*
+ * pstat_forward followed by pstat_backward in one pass over the logits
+ * (the pages' forward+backward unit, reusing cross-entropy forward and
+ * backward together; here as one kernel).  Results are bit-identical to the
+ * two calls with the same arguments; the logits are read from HBM once (each
+ * CTA re-reads a row's chunks from L2 for the gradient), so a bf16 token
+ * moves 4V bytes instead of 6V.  No workspace: a row's chunk records live in
+ * shared memory.
+ *   Arguments as in pstat_forward / pstat_backward; out_dlogits [T, ld_out]
+ *   is required, out_logprob / out_entropy / out_rowstats may be NULL.
+ *   The shard plan may have at most 256 chunks per row (PSTAT_ERR_SHAPE).
+ */
+PSTAT_API int pstat_forward_backward(const void* logits, pstat_dtype dt, int64_t T, int64_t V,
+                                     int64_t ld, const int64_t* labels, int64_t ignore_index,
+                                     const float* weights, const int64_t* shard_bounds,
+                                     int n_shards, float* out_logprob, float* out_entropy,
+                                     float* out_rowstats, void* out_dlogits, pstat_dtype out_dt,
+                                     int64_t ld_out, int* dev_error, pstat_stream_t stream);
+
+/*
  * Workspace bytes for the fused lm_head entry points (T tokens, V vocab
  * rows, hidden size d).
  */

@@ -1,0 +1,125 @@
+"""pstat_forward_backward (one pass over the logits) against the two-call
+path pstat_forward + pstat_backward -- bit for bit -- and against the float64
+oracle directly, on the edge cases and at full size."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import assert_forward_close, assert_grad_close, to_oracle
+
+pytestmark = pytest.mark.gpu
+IGN = -100
+
+
+def _bits(x):
+    x = x.contiguous()
+    return x.view(torch.int16 if x.element_size() == 2 else torch.int32)
+
+
+def _same_as_two_calls(pstat, z, y, w, bounds=None, out_dtype=None):
+    e1 = pstat.new_error_flag(z.device)
+    e2 = pstat.new_error_flag(z.device)
+    lp, ent, rs = pstat.forward(z, y, IGN, bounds, dev_error=e1)
+    g = pstat.backward(z, y, w, rs, IGN, out_dtype=out_dtype, dev_error=e1)
+    lp2, ent2, rs2, g2 = pstat.forward_backward(z, y, w, IGN, bounds, out_dtype, dev_error=e2)
+    torch.cuda.synchronize()
+    for a, b, name in ((lp, lp2, "logprob"), (ent, ent2, "entropy"), (rs, rs2, "rowstats"),
+                       (g, g2, "dlogits")):
+        assert torch.equal(_bits(a), _bits(b)), name
+    assert e1.item() == e2.item()
+    return lp2, ent2, rs2, g2, e2.item()
+
+
+@pytest.mark.parametrize("dtype,out_dtype", [(torch.bfloat16, torch.bfloat16),
+                                             (torch.float32, torch.float32),
+                                             (torch.float32, torch.bfloat16)])
+@pytest.mark.parametrize("V,bounds", [(10007, None), (10007, [0, 513, 6000, 10007]),
+                                      (1001, None), (8, None), (7, None), (1, None),
+                                      (151936, [0, 50000, 100000, 151936])])
+def test_fused_bitwise_equals_two_calls(cuda_lib, dtype, out_dtype, V, bounds):
+    g = torch.Generator(device="cuda").manual_seed(V + 17)
+    T = 300
+    z = (2.5 * torch.randn(T, V, generator=g, device="cuda")).float()
+    if V > 20:
+        z[5, : V // 3] = -math.inf          # masked first third
+        z[6, ::5] = -math.inf
+    z = z.to(dtype)
+    y = torch.randint(0, V, (T,), generator=g, device="cuda")
+    y[3] = IGN
+    if V > 20:
+        y[6] = 1
+    w = torch.randn(T, generator=g, device="cuda")
+    w[4] = 0.0
+    lp, ent, rs, gg, err = _same_as_two_calls(cuda_lib, z, y, w, bounds, out_dtype)
+    assert err == 0
+    zo, yo = to_oracle(z), y.cpu().numpy()
+    ref = oracle.forward(zo, yo, IGN)
+    assert_forward_close(lp, ent, ref, dtype, what=f"fused V={V}")
+    gref = oracle.backward(zo, yo, w.double().cpu().numpy(), IGN)
+    assert_grad_close(gg, gref, out_dtype, f"fused V={V}")
+
+
+@pytest.mark.parametrize("offset", [1, 3])
+def test_fused_unaligned_rows_and_outputs(cuda_lib, offset):
+    g = torch.Generator(device="cuda").manual_seed(offset)
+    T, V = 40, 9001
+    big = (2.0 * torch.randn(T, V + offset + 5, generator=g, device="cuda")).to(torch.bfloat16)
+    z = big[:, offset:offset + V]
+    y = torch.randint(0, V, (T,), generator=g, device="cuda")
+    w = torch.randn(T, generator=g, device="cuda")
+    lp, ent, rs = cuda_lib.forward(z, y, IGN)
+    g1 = cuda_lib.backward(z, y, w, rs, IGN)
+    outbig = torch.empty(T, V + 3, dtype=torch.bfloat16, device="cuda")
+    dl = outbig[:, 1:1 + V]
+    lp2, ent2, rs2, g2 = cuda_lib.forward_backward(z, y, w, IGN, dlogits=dl)
+    torch.cuda.synchronize()
+    assert torch.equal(_bits(lp), _bits(lp2)) and torch.equal(_bits(ent), _bits(ent2))
+    assert torch.equal(_bits(g1), _bits(g2))
+
+
+def test_fused_device_errors(cuda_lib):
+    T, V = 4, 3000
+    z = torch.randn(T, V, device="cuda")
+    z[2] = -math.inf
+    y = torch.tensor([5, V, 3, -7], device="cuda")
+    w = torch.ones(T, device="cuda")
+    lp, ent, rs, g, err = _same_as_two_calls(cuda_lib, z, y, w)
+    assert err & cuda_lib.DEV_BAD_LABEL and err & cuda_lib.DEV_EMPTY_ROW
+    assert torch.all(torch.isnan(g[1])) and torch.all(torch.isnan(g[2]))
+
+
+def test_fused_tiny_config_against_oracle(cuda_lib):
+    from vocab_wide_token_gb300 import inputs
+
+    d = inputs.tiny(0, "cuda")
+    z, y, w, b = d["logits"], d["labels"], d["weights"], d["shard_bounds"]
+    lp, ent, rs, g = cuda_lib.forward_backward(z, y, w, IGN, b, torch.float32)
+    torch.cuda.synchronize()
+    zo, yo = z.cpu().numpy(), y.cpu().numpy()
+    assert_forward_close(lp, ent, oracle.forward(zo, yo, IGN), torch.float32, what="tiny")
+    assert_grad_close(g, oracle.backward(zo, yo, w.double().cpu().numpy(), IGN), torch.float32,
+                      "tiny")
+
+
+def test_fused_full_size_and_batch_invariance(cuda_lib):
+    """T=8192, V=151936 bf16 (the benchmark workload): bitwise equal to the
+    two-call path on every row; sampled rows alone give the same bits."""
+    from vocab_wide_token_gb300 import inputs
+
+    d = inputs.fwdbwd_workload(2, "cuda")
+    z, y, w = d["logits"], d["labels"], d["weights"]
+    lp, ent, rs, g, err = _same_as_two_calls(cuda_lib, z, y, w)
+    assert err == 0
+    for p in (0, 4095, 8191):
+        l1, e1, r1, g1 = cuda_lib.forward_backward(z[p:p + 1], y[p:p + 1], w[p:p + 1])
+        torch.cuda.synchronize()
+        assert torch.equal(_bits(l1), _bits(lp[p:p + 1]))
+        assert torch.equal(_bits(g1[0]), _bits(g[p]))
+    rows = np.array([0, 1, 77, 4095, 8191])
+    zo, yo = to_oracle(z[rows]), y[rows].cpu().numpy()
+    assert_forward_close(lp[rows], ent[rows], oracle.forward(zo, yo, IGN), torch.bfloat16)
+    assert_grad_close(g[rows], oracle.backward(zo, yo, w[rows].double().cpu().numpy(), IGN),
+                      torch.bfloat16, "full")

@@ -1,0 +1,522 @@
+// fused.cu -- pstat_forward_backward: logprob, entropy, (M, ln S) and the
+// weighted backward dlogits = w (onehot(y) - softmax(z)) in one kernel.
+//
+// Calling pstat_forward then pstat_backward streams the logits from HBM
+// twice (6V bytes per bf16 token with the dlogits write).  Here each CTA owns
+// whole rows and passes over every row twice back to back:
+//   pass 1  streams the row's chunks from HBM (bulk copies with an L2
+//           evict-last hint) and forms each chunk's (m, s, u) record, exactly
+//           as the chunk-statistics kernel does, into shared memory;
+//           the warp that finishes the row's last chunk folds the records in
+//           the fixed order of the combine kernel and publishes (M, ln S);
+//   pass 2  streams the same chunks again -- now from L2 -- and writes
+//           dlogits with the element-wise arithmetic of the backward kernel.
+// HBM sees 4V bytes per token (read once, write once).  Rows are dealt to
+// CTAs round robin; within a CTA each warp runs pass 1 of a row, then pass 2
+// of the row before it, keeping its 2-slot ring of bulk copies full across
+// passes and rows, so nobody waits for a row's fold.  Every record, fold
+// and gradient element is computed by the same code as in the two-call path,
+// so the results are bit-identical to pstat_forward + pstat_backward.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "chunk_math.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace pstat {
+namespace {
+
+constexpr int kFbMaxChunks = 256;  // chunk records per row held in shared memory
+
+struct RowInfo {
+    float M, log2S, w;
+    int mode;  // 0: all-zero row, 1: NaN row, 2: compute
+    long long y;
+    long long pad;
+};
+
+constexpr size_t kRingBytes = (size_t)kWarps * kStages * kSlotBytes;
+constexpr size_t kBarBytes = (size_t)kWarps * kStages * sizeof(uint64_t);
+constexpr size_t kRecOff = kRingBytes + kBarBytes;
+constexpr size_t kInfoOff = kRecOff + 2 * kFbMaxChunks * sizeof(float4);
+constexpr size_t kReadyOff = kInfoOff + 2 * sizeof(RowInfo);
+constexpr size_t kCountOff = kReadyOff + 2 * sizeof(uint64_t);
+constexpr size_t kFusedSmem = kCountOff + 2 * sizeof(int);
+
+template <typename E>
+struct OutVec;
+template <>
+struct OutVec<uint16_t> {  // bf16 output, round to nearest even
+    template <int N>
+    __device__ static void store(uint16_t* p, const float (&g)[N]) {
+        if constexpr (N == 8) {
+            uint4 q;
+            q.x = bf2_pack_rn(g[0], g[1]);
+            q.y = bf2_pack_rn(g[2], g[3]);
+            q.z = bf2_pack_rn(g[4], g[5]);
+            q.w = bf2_pack_rn(g[6], g[7]);
+            __stcs(reinterpret_cast<uint4*>(p), q);
+        } else {
+            uint2 q;
+            q.x = bf2_pack_rn(g[0], g[1]);
+            q.y = bf2_pack_rn(g[2], g[3]);
+            __stcs(reinterpret_cast<uint2*>(p), q);
+        }
+    }
+    __device__ static uint16_t one(float g) { return (uint16_t)(bf2_pack_rn(g, 0.f) & 0xFFFFu); }
+};
+template <>
+struct OutVec<float> {
+    template <int N>
+    __device__ static void store(float* p, const float (&g)[N]) {
+#pragma unroll
+        for (int i = 0; i < N; i += 4)
+            __stcs(reinterpret_cast<float4*>(p + i), make_float4(g[i], g[i + 1], g[i + 2], g[i + 3]));
+    }
+    __device__ static float one(float g) { return g; }
+};
+
+// The backward kernel's element arithmetic for N = 4 or 8 elements.
+template <int N>
+__device__ __forceinline__ void grad_vec(const float (&x)[N], const RowInfo& ri, int64_t col0,
+                                         int64_t y, float (&g)[N]) {
+    float p[N];
+    if constexpr (N == 8) {
+        prob8(x, ri.M, ri.log2S, p);
+    } else {
+        float x8[8] = {x[0], x[1], x[2], x[3], x[0], x[1], x[2], x[3]};
+        float p8[8];
+        prob8(x8, ri.M, ri.log2S, p8);
+#pragma unroll
+        for (int i = 0; i < N; ++i) p[i] = p8[i];
+    }
+    const float negw = -ri.w;
+    const uint64_t nw = f2_pack(negw, negw);
+#pragma unroll
+    for (int i = 0; i < N; i += 2) f2_unpack(f2_mul(f2_pack(p[i], p[i + 1]), nw), g[i], g[i + 1]);
+    const int64_t r = y - col0;
+    if (r >= 0 && r < N) {
+#pragma unroll
+        for (int e = 0; e < N; ++e)
+            if (e == r) g[e] = fmaf(negw, p[e], ri.w);  // w (1 - p_y)
+    }
+}
+
+// Same without the label column (the caller knows it is not in the vector).
+template <int N>
+__device__ __forceinline__ void grad_vec_nolabel(const float (&x)[N], const RowInfo& ri,
+                                                 float (&g)[N]) {
+    float p[N];
+    if constexpr (N == 8) {
+        prob8(x, ri.M, ri.log2S, p);
+    } else {
+        float x8[8] = {x[0], x[1], x[2], x[3], x[0], x[1], x[2], x[3]};
+        float p8[8];
+        prob8(x8, ri.M, ri.log2S, p8);
+#pragma unroll
+        for (int i = 0; i < N; ++i) p[i] = p8[i];
+    }
+    const float negw = -ri.w;
+    const uint64_t nw = f2_pack(negw, negw);
+#pragma unroll
+    for (int i = 0; i < N; i += 2) f2_unpack(f2_mul(f2_pack(p[i], p[i + 1]), nw), g[i], g[i + 1]);
+}
+
+template <typename Ein>
+__device__ __forceinline__ void unpack_vec(const uint4& v, float (&x)[Elem<Ein>::kVec]);
+template <>
+__device__ __forceinline__ void unpack_vec<uint16_t>(const uint4& v, float (&x)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        x[2 * i] = bf2_lo(w[i]);
+        x[2 * i + 1] = bf2_hi(w[i]);
+    }
+}
+template <>
+__device__ __forceinline__ void unpack_vec<float>(const uint4& v, float (&x)[4]) {
+    x[0] = __uint_as_float(v.x);
+    x[1] = __uint_as_float(v.y);
+    x[2] = __uint_as_float(v.z);
+    x[3] = __uint_as_float(v.w);
+}
+
+template <typename Ein, typename Eout>
+__global__ void __launch_bounds__(kWarps * 32, 1)
+    fwdbwd_kernel(const Ein* __restrict__ logits, int64_t T, int64_t V, int64_t ld,
+                  const __grid_constant__ ShardPlan plan, const int64_t* __restrict__ labels,
+                  int64_t ignore_index, const float* __restrict__ weights,
+                  float* __restrict__ logprob, float* __restrict__ entropy,
+                  float* __restrict__ rowstats, Eout* __restrict__ out, int64_t ld_out,
+                  int* __restrict__ dev_error) {
+    constexpr int kVec = Elem<Ein>::kVec;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    uint8_t* slots = smem + (size_t)warp * kStages * kSlotBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRingBytes) + warp * kStages;
+    float4* records = reinterpret_cast<float4*>(smem + kRecOff);
+    RowInfo* info = reinterpret_cast<RowInfo*>(smem + kInfoOff);
+    uint64_t* ready = reinterpret_cast<uint64_t*>(smem + kReadyOff);
+    int* counter = reinterpret_cast<int*>(smem + kCountOff);
+
+    const int nc = plan.n_chunks;
+    const int active = nc < kWarps ? nc : kWarps;  // warps that own chunks of any one row
+    if (lane == 0) {
+        for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+    }
+    if (threadIdx.x == 0) {
+        mbar_init(&ready[0], 1);
+        mbar_init(&ready[1], 1);
+        counter[0] = 0;
+        counter[1] = 0;
+    }
+    fence_mbar_init();
+    __syncthreads();
+    // Rotating the chunk assignment keeps every warp in every row only when a
+    // row has at least one chunk per warp; with fewer chunks the assignment is
+    // fixed (warp w owns chunk w of every row) and the other warps leave.  In
+    // both cases each working warp owns a chunk of every row, so it arrives
+    // for every row's fold and reads every row's statistics before the
+    // double-buffered records and row data are reused two rows later.
+    const bool rotate = nc >= kWarps;
+    if (!rotate && warp >= nc) return;
+
+    const int64_t nrows = (T > (int64_t)blockIdx.x) ? (T - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    const uint64_t pol_keep = policy_evict_last();
+    const uint64_t pol_once = policy_evict_first();
+
+    // A warp's work is a sequence of segments: for k = 0 .. nrows, pass 1 of
+    // the CTA's row k, then pass 2 of its row k - 1.  So a row's statistics
+    // are folded while the warps already stream the next row, and pass 2
+    // never waits on the slowest warp.  Chunks are dealt round robin over the
+    // concatenated chunk stream of the CTA's rows: warp w owns chunks
+    // g0, g0 + 12, ... of row r, g0 = (w - r nc) mod 12, so the rows' spare
+    // chunks rotate over the warps (when rotating, see above).
+    struct Cursor {
+        int64_t k;
+        int pass, i, cnt, g0;
+    };
+    auto load_segment = [&](Cursor& c) {
+        const int64_t r = c.k - c.pass;
+        if (r < 0 || r >= nrows) {
+            c.cnt = 0;
+            return;
+        }
+        const int rot = rotate ? (int)((r * nc) % kWarps) : 0;
+        c.g0 = (warp - rot + kWarps) % kWarps;
+        c.cnt = c.g0 < nc ? (nc - c.g0 + kWarps - 1) / kWarps : 0;
+    };
+    auto settle = [&](Cursor& c) {  // first position at or after c that holds a chunk
+        while (c.k <= nrows) {
+            load_segment(c);
+            if (c.i < c.cnt) return;
+            c.i = 0;
+            if (c.pass == 0) {
+                c.pass = 1;
+            } else {
+                c.pass = 0;
+                ++c.k;
+            }
+        }
+    };
+    auto advance = [&](Cursor& c) {
+        ++c.i;
+        settle(c);
+    };
+    auto done = [&](const Cursor& c) { return c.k > nrows; };
+
+    struct Task {
+        int64_t r, t;  // the CTA's row index, token row
+        int g;
+        bool bulk;     // served by a bulk copy into its slot
+        const Ein* src;
+        int64_t start;
+        int len;
+    };
+    auto task_of = [&](const Cursor& c) {
+        Task tk;
+        tk.r = c.k - c.pass;
+        tk.g = c.g0 + kWarps * c.i;
+        tk.t = blockIdx.x + tk.r * gridDim.x;
+        chunk_span(plan, tk.g, tk.start, tk.len);
+        tk.src = logits + tk.t * ld + tk.start;
+        tk.bulk = ((reinterpret_cast<uintptr_t>(tk.src) & 15u) == 0) &&
+                  ((((size_t)tk.len * sizeof(Ein)) & 15u) == 0);
+        return tk;
+    };
+    auto issue = [&](const Cursor& c, int64_t pos) {
+        const Task tk = task_of(c);
+        if (tk.bulk && lane == 0) {
+            const int slot = (int)(pos % kStages);
+            const uint32_t bytes = (uint32_t)tk.len * (uint32_t)sizeof(Ein);
+            // pass 1: the row is read again by pass 2, so keep it in L2
+            mbar_arrive_expect_tx(&bars[slot], bytes);
+            bulk_g2s_evict_first(slots + (size_t)slot * kSlotBytes, tk.src, bytes, &bars[slot],
+                                 c.pass == 0 ? pol_keep : pol_once);
+        }
+    };
+
+    Cursor ci = {0, 0, 0, 0, 0};  // next position to issue
+    settle(ci);
+    int64_t pi = 0;
+    for (int s = 0; s < kStages && !done(ci); ++s, ++pi) {
+        issue(ci, pi);
+        advance(ci);
+    }
+
+    Cursor cc = {0, 0, 0, 0, 0};  // position being consumed
+    settle(cc);
+    int64_t pc = 0;
+    uint32_t phase = 0;  // parity bit per ring slot
+    bool failed = false;
+    RowInfo ri = {0.f, 0.f, 0.f, 0, 0, 0};
+    while (!done(cc)) {
+        const Task tk = task_of(cc);
+        const int b = (int)(tk.r & 1);
+        const int slot = (int)(pc % kStages);
+        Ein* buf = reinterpret_cast<Ein*>(slots + (size_t)slot * kSlotBytes);
+        const int len = tk.len;
+        const int64_t start = tk.start;
+
+        if (cc.pass == 1 && cc.i == 0) {
+            // (M, ln S) of this row, published by the warp that folded it.
+            bool ok = mbar_wait_bounded(&ready[b], (uint32_t)((tk.r >> 1) & 1), kWaitLimitNs);
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            if (!ok) {
+                failed = true;
+                break;
+            }
+            ri = info[b];
+        }
+        const bool need_data = cc.pass == 0 || ri.mode == 2;
+        if (tk.bulk) {
+            bool ok = mbar_wait_bounded(&bars[slot], (phase >> slot) & 1u, kWaitLimitNs);
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            if (!ok) {
+                failed = true;
+                break;
+            }
+            phase ^= 1u << slot;
+        } else if (need_data) {
+            // Unaligned chunk: element loads, padded with -inf to a whole vector.
+            const int padded = (len + kVec - 1) / kVec * kVec;
+            for (int k = lane; k < padded; k += 32)
+                buf[k] = (k < len) ? tk.src[k] : Elem<Ein>::neg_inf();
+            __syncwarp();
+        }
+        const int nvec = (len + kVec - 1) / kVec;
+        uint4 q[kVecPerLane];
+        if (need_data) load_chunk_regs<Ein>(buf, len, lane, q);
+        __syncwarp();
+        fence_proxy_async_smem();  // our reads of the slot precede the next bulk write into it
+        if (!done(ci)) {
+            issue(ci, pi);
+            advance(ci);
+            ++pi;
+        }
+
+        if (cc.pass == 0) {
+            const float4 rec = reduce_regs(q, (Ein*)nullptr);
+            if (lane == 0) records[b * kFbMaxChunks + tk.g] = rec;
+            if (cc.i == cc.cnt - 1) {
+                // This warp's last chunk of the row: the last warp to get here folds.
+                __syncwarp();
+                if (lane == 0) {
+                    __threadfence_block();
+                    const int arrived = atomicAdd(&counter[b], 1);
+                    if (arrived == active - 1) {
+                        __threadfence_block();
+                        counter[b] = 0;
+                        const float4 st = fold_row(records + b * kFbMaxChunks, plan);
+                        const float M = st.x, S = st.y, U = st.z;
+                        const int64_t t = tk.t;
+                        const int64_t y = labels ? labels[t] : ignore_index;
+                        const float w = weights ? weights[t] : 1.f;
+                        int err = 0;
+                        float lnS, H, lp;
+                        RowInfo nr;
+                        nr.w = w;
+                        if (!(M > -INFINITY)) {
+                            err |= PSTAT_DEV_EMPTY_ROW;
+                            lnS = NAN;
+                            H = NAN;
+                            lp = NAN;
+                        } else {
+                            lnS = logf(S);
+                            H = lnS - U / S;
+                            if (y == ignore_index) {
+                                lp = 0.f;
+                            } else if (y < 0 || y >= V) {
+                                err |= PSTAT_DEV_BAD_LABEL;
+                                lp = NAN;
+                                H = NAN;
+                            } else {
+                                const float zy = Elem<Ein>::to_float(logits[t * ld + y]);
+                                lp = (zy - M) - lnS;
+                            }
+                        }
+                        if (y == ignore_index || w == 0.f)
+                            nr.mode = 0;
+                        else if (err)
+                            nr.mode = 1;
+                        else
+                            nr.mode = 2;
+                        nr.M = M;
+                        nr.log2S = lnS * kLog2e;
+                        nr.y = y;
+                        nr.pad = 0;
+                        info[b] = nr;
+                        if (logprob) logprob[t] = lp;
+                        if (entropy) entropy[t] = H;
+                        if (rowstats) reinterpret_cast<float2*>(rowstats)[t] = make_float2(M, lnS);
+                        if (err && dev_error) atomicOr(dev_error, err);
+                        mbar_arrive(&ready[b]);  // release: records, info visible to waiters
+                    }
+                }
+                __syncwarp();
+            }
+        } else {
+            // dlogits of this chunk: columns [start, start + len) of row t
+            Eout* dst = out + tk.t * ld_out + start;
+            const int64_t y = ri.y;
+            const bool vec_ok = ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0) &&
+                                (len % kVec == 0);
+            if (ri.mode == 2) {
+                const bool has_y = y >= start && y < start + len;
+                if (vec_ok && nvec == 32 * kVecPerLane && !has_y) {
+                    // full aligned chunk without the label: no per-vector tests
+                    Eout* d = dst + lane * kVec;
+#pragma unroll
+                    for (int jj = 0; jj < kVecPerLane; ++jj) {
+                        float x[kVec], gv[kVec];
+                        unpack_vec<Ein>(q[jj], x);
+                        grad_vec_nolabel<kVec>(x, ri, gv);
+                        OutVec<Eout>::template store<kVec>(d + 32 * kVec * jj, gv);
+                    }
+                } else {
+#pragma unroll
+                    for (int jj = 0; jj < kVecPerLane; ++jj) {
+                        const int k = lane + 32 * jj;
+                        if (k >= nvec) break;
+                        float x[kVec], gv[kVec];
+                        unpack_vec<Ein>(q[jj], x);
+                        grad_vec<kVec>(x, ri, start + (int64_t)k * kVec, y, gv);
+                        if (vec_ok) {
+                            OutVec<Eout>::template store<kVec>(dst + (int64_t)k * kVec, gv);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < kVec; ++e)
+                                if (k * kVec + e < len)
+                                    dst[(int64_t)k * kVec + e] = OutVec<Eout>::one(gv[e]);
+                        }
+                    }
+                }
+            } else {
+                const float fill = (ri.mode == 0) ? 0.f : NAN;
+                float gv[kVec];
+#pragma unroll
+                for (int e = 0; e < kVec; ++e) gv[e] = fill;
+                for (int k = lane; k < nvec; k += 32) {
+                    if (vec_ok) {
+                        OutVec<Eout>::template store<kVec>(dst + (int64_t)k * kVec, gv);
+                    } else {
+                        for (int e = 0; e < kVec; ++e)
+                            if (k * kVec + e < len) dst[(int64_t)k * kVec + e] = OutVec<Eout>::one(fill);
+                    }
+                }
+            }
+        }
+        advance(cc);
+        ++pc;
+    }
+    if (failed) {
+        if (lane == 0 && dev_error) atomicOr(dev_error, PSTAT_DEV_TIMEOUT);
+        // Drain copies still in flight into this CTA's shared memory before leaving.
+        for (int64_t p = pc; p < pi; ++p) {
+            if (task_of(cc).bulk) {
+                const int slot = (int)(p % kStages);
+                mbar_wait_bounded(&bars[slot], (phase >> slot) & 1u, kWaitLimitNs);
+                phase ^= 1u << slot;
+            }
+            advance(cc);
+        }
+    }
+}
+
+template <typename Ein, typename Eout>
+cudaError_t launch_fused_t(const Ein* logits, int64_t T, int64_t V, int64_t ld,
+                           const ShardPlan& plan, const int64_t* labels, int64_t ignore_index,
+                           const float* weights, float* logprob, float* entropy, float* rowstats,
+                           Eout* out, int64_t ld_out, int* dev_error, const DeviceInfo& dev,
+                           cudaStream_t stream) {
+    static std::atomic<bool> configured[64];
+    int d = 0;
+    cudaGetDevice(&d);
+    if (d >= 64 || !configured[d].load(std::memory_order_acquire)) {
+        const cudaError_t e = cudaFuncSetAttribute(fwdbwd_kernel<Ein, Eout>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)kFusedSmem);
+        if (e != cudaSuccess) return e;
+        if (d < 64) configured[d].store(true, std::memory_order_release);
+    }
+    const int64_t grid = T < dev.sm_count ? T : dev.sm_count;
+    fwdbwd_kernel<Ein, Eout><<<(unsigned)grid, kWarps * 32, kFusedSmem, stream>>>(
+        logits, T, V, ld, plan, labels, ignore_index, weights, logprob, entropy, rowstats, out,
+        ld_out, dev_error);
+    return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace pstat
+
+using namespace pstat;
+
+extern "C" int pstat_forward_backward(const void* logits, pstat_dtype dt, int64_t T, int64_t V,
+                                      int64_t ld, const int64_t* labels, int64_t ignore_index,
+                                      const float* weights, const int64_t* shard_bounds,
+                                      int n_shards, float* out_logprob, float* out_entropy,
+                                      float* out_rowstats, void* out_dlogits, pstat_dtype out_dt,
+                                      int64_t ld_out, int* dev_error, pstat_stream_t stream) {
+    if ((dt != PSTAT_F32 && dt != PSTAT_BF16) || (out_dt != PSTAT_F32 && out_dt != PSTAT_BF16))
+        return PSTAT_ERR_DTYPE;
+    if (dt == PSTAT_BF16 && out_dt == PSTAT_F32) return PSTAT_ERR_DTYPE;
+    if (T < 0 || V < 1 || ld < V || ld_out < V) return PSTAT_ERR_SHAPE;
+    ShardPlan plan;
+    int rc = make_plan(V, dt == PSTAT_BF16 ? PSTAT_CHUNK_BF16 : PSTAT_CHUNK_F32, shard_bounds,
+                       n_shards, &plan);
+    if (rc != PSTAT_OK) return rc;
+    if (plan.n_chunks > kFbMaxChunks) return PSTAT_ERR_SHAPE;
+    if (T == 0) return PSTAT_OK;
+    if (!logits || !out_dlogits) return PSTAT_ERR_NULLPTR;
+    const size_t ein = dt == PSTAT_BF16 ? 2 : 4, eout = out_dt == PSTAT_BF16 ? 2 : 4;
+    if ((reinterpret_cast<uintptr_t>(logits) % ein) != 0 ||
+        (reinterpret_cast<uintptr_t>(out_dlogits) % eout) != 0)
+        return PSTAT_ERR_ALIGN;
+    if ((out_rowstats && (reinterpret_cast<uintptr_t>(out_rowstats) & 7u)) ||
+        (labels && (reinterpret_cast<uintptr_t>(labels) & 7u)) ||
+        (weights && (reinterpret_cast<uintptr_t>(weights) & 3u)))
+        return PSTAT_ERR_ALIGN;
+    DeviceInfo dev;
+    rc = device_info(&dev);
+    if (rc != PSTAT_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (dt == PSTAT_BF16)
+        e = launch_fused_t(static_cast<const uint16_t*>(logits), T, V, ld, plan, labels,
+                           ignore_index, weights, out_logprob, out_entropy, out_rowstats,
+                           static_cast<uint16_t*>(out_dlogits), ld_out, dev_error, dev, st);
+    else if (out_dt == PSTAT_BF16)
+        e = launch_fused_t(static_cast<const float*>(logits), T, V, ld, plan, labels,
+                           ignore_index, weights, out_logprob, out_entropy, out_rowstats,
+                           static_cast<uint16_t*>(out_dlogits), ld_out, dev_error, dev, st);
+    else
+        e = launch_fused_t(static_cast<const float*>(logits), T, V, ld, plan, labels,
+                           ignore_index, weights, out_logprob, out_entropy, out_rowstats,
+                           static_cast<float*>(out_dlogits), ld_out, dev_error, dev, st);
+    return e == cudaSuccess ? PSTAT_OK : PSTAT_ERR_CUDA;
+}

@@ -40,6 +40,9 @@ _lib.pstat_forward_noalloc.restype = _i32
 _lib.pstat_backward.argtypes = [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _vp,
                                 _i32, _i64, _vp, _sz, _vp, _vp]
 _lib.pstat_backward.restype = _i32
+_lib.pstat_forward_backward.argtypes = [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _i32,
+                                        _vp, _vp, _vp, _vp, _i32, _i64, _vp, _vp]
+_lib.pstat_forward_backward.restype = _i32
 _lib.pstat_lmhead_workspace_size.argtypes = [_i64, _i64, _i64, ctypes.POINTER(_sz)]
 _lib.pstat_lmhead_workspace_size.restype = _i32
 _lib.pstat_lmhead_fused.argtypes = [_vp, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _vp,
@@ -221,6 +224,39 @@ def backward(logits: torch.Tensor, labels: torch.Tensor | None, weights: torch.T
                                _stream(dev)),
            "pstat_backward")
     return out
+
+
+def forward_backward(logits: torch.Tensor, labels: torch.Tensor | None,
+                     weights: torch.Tensor | None, ignore_index: int = -100, shard_bounds=None,
+                     out_dtype: torch.dtype | None = None, *, out=None, dlogits=None,
+                     dev_error=None):
+    """pstat_forward and pstat_backward in one pass over the logits (same
+    results, bit for bit).  Returns (logprob, entropy, rowstats, dlogits)."""
+    T, V, ld = _rows(logits)
+    dev = logits.device
+    lab = _labels(labels, T, dev)
+    out_dtype = out_dtype or logits.dtype
+    if out is None:
+        lp = torch.empty(T, dtype=torch.float32, device=dev)
+        ent = torch.empty(T, dtype=torch.float32, device=dev)
+        rs = torch.empty(T, 2, dtype=torch.float32, device=dev)
+    else:
+        lp, ent, rs = out
+    if dlogits is None:
+        dlogits = torch.empty(T, V, dtype=out_dtype, device=dev)
+    if dlogits.dim() != 2 or dlogits.shape != (T, V) or dlogits.stride(1) != 1:
+        raise ValueError("dlogits must be [T, V] with contiguous rows")
+    ld_out = dlogits.stride(0) if T > 1 else V
+    w = None if weights is None else weights.contiguous()
+    if w is not None and (w.dtype != torch.float32 or w.shape != (T,)):
+        raise ValueError("weights must be float32 [T]")
+    arr, ns = _bounds(shard_bounds, V)
+    _check(_lib.pstat_forward_backward(_ptr(logits), _dtype_code(logits), T, V, ld, _ptr(lab),
+                                       int(ignore_index), _ptr(w), arr, ns, _ptr(lp), _ptr(ent),
+                                       _ptr(rs), _ptr(dlogits), _dtype_code(dlogits), ld_out,
+                                       _ptr(dev_error), _stream(dev)),
+           "pstat_forward_backward")
+    return lp, ent, rs, dlogits
 
 
 def lmhead_workspace_size(T: int, V: int, d: int) -> int:
