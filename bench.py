@@ -467,7 +467,7 @@ def bench_lmhead(pstat, dev, tflops, tflops_sus, peak_kind, T=16384, steps=3, wa
     flop_b = 6.0 * T * V * dm
     af = flop_f / (fwd_ms / 1e3) / 1e12
     ab = flop_b / (bwd_ms / 1e3) / 1e12
-    n_chunks = (V + 4095) // 4096
+    n_chunks = (V + 8191) // 8192  # vocabulary columns staged per backward chunk
     return {"status": "ok", "workload": f"hidden [{T}, {dm}] x W [{V}, {dm}] bf16, sampled labels",
             "forward_ms": fwd_ms, "forward_tokens_per_s": T / (fwd_ms / 1e3),
             "backward_ms": bwd_ms, "backward_tokens_per_s": T / (bwd_ms / 1e3),

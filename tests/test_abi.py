@@ -101,3 +101,56 @@ def test_backward_argument_checks(lib):
     assert bwd(out=0) == -1
     assert bwd(rowstats=0) == -6           # recompute needs a workspace
     assert bwd(out=0x4001) == -5
+
+
+def test_forward_backward_argument_checks(lib):
+    def fb(dt=1, out_dt=1, T=4, V=100, ld=100, ld_out=100, logits=0x1000, out=0x4000,
+           bounds=None, ns=1):
+        b = None if bounds is None else (ctypes.c_int64 * len(bounds))(*bounds)
+        return lib.pstat_forward_backward(ctypes.c_void_p(logits), dt, T, V, ld, None, -100, None,
+                                          b, ns, None, None, None, ctypes.c_void_p(out), out_dt,
+                                          ld_out, None, None)
+    assert fb(dt=9) == -4
+    assert fb(dt=1, out_dt=0) == -4
+    assert fb(ld_out=10) == -2
+    assert fb(out=0) == -1
+    assert fb(logits=0x1001) == -5
+    assert fb(T=0, logits=0, out=0) == 0
+    # more than 256 chunks per row is refused (records live in shared memory)
+    assert fb(V=4096 * 257, ld=4096 * 257, ld_out=4096 * 257) == -2
+    assert fb(bounds=[0, 60, 50, 100], ns=3) == -3
+
+
+def test_noalloc_argument_checks(lib):
+    def na(T=4, V=100, logits=0x1000):
+        return lib.pstat_forward_noalloc(ctypes.c_void_p(logits), 1, T, V, V, None, -100, None, 1,
+                                         None, None, None, None, None)
+    assert na(V=0) == -2
+    assert na(logits=0) == -1
+    assert na(T=0, logits=0) == 0
+    # beyond the fixed 8 MiB scratch: 16-byte records per row and chunk
+    assert na(T=(8 << 20) // (16 * 38) + 1, V=151936) == -6
+
+
+def test_lmhead_argument_checks(lib):
+    n = ctypes.c_size_t(0)
+    assert lib.pstat_lmhead_workspace_size(16384, 151936, 4096, ctypes.byref(n)) == 0
+    assert n.value > 16384 * 38 * 16
+    assert lib.pstat_lmhead_workspace_size(16, 100, 100, ctypes.byref(n)) == -2   # d % 64
+    def fw(h=0x1000, W=0x2000, T=4, V=100, d=128, ws=0x3000, ws_bytes=1 << 20):
+        return lib.pstat_lmhead_fused(ctypes.c_void_p(h), ctypes.c_void_p(W), T, V, d, None, -100,
+                                      None, None, None, ctypes.c_void_p(ws), ws_bytes, None, None)
+    assert fw(d=96) == -2
+    assert fw(h=0) == -1
+    assert fw(W=0x2008) == -5          # 16-byte alignment for TMA
+    assert fw(ws=0) == -6
+    assert fw(T=0, h=0, W=0) == 0
+    def bw(rowstats=0x5000, dh=0x6000, dW=0x7000, ws=0x8000, ws_bytes=1 << 30):
+        return lib.pstat_lmhead_backward(ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000), 4, 100,
+                                         128, None, -100, None, ctypes.c_void_p(rowstats),
+                                         ctypes.c_void_p(dh), ctypes.c_void_p(dW),
+                                         ctypes.c_void_p(ws), ws_bytes, None, None)
+    assert bw(rowstats=0) == -1        # the backward needs (M, ln S) from the forward
+    assert bw(dW=0x7004) == -5
+    assert bw(ws_bytes=16) == -6
+    assert bw(ws=0x8010) == -5         # 1024-byte aligned workspace

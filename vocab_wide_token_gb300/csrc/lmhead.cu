@@ -7,7 +7,7 @@
 // global memory.  The fixed-order combine kernel then gives logprob, entropy
 // and (M, ln S).
 //
-// Backward, per 4096-column vocabulary chunk c (the chunked lm_head of TRL PR
+// Backward, per 8192-column vocabulary chunk c (the chunked lm_head of TRL PR
 // #6949 "ZeroSyncGRPOTrainer": GEMMs in a 16-bit dtype, accumulation in fp32
 // buffers):
 //   1. recompute the chunk's logits tile by tile and turn them on chip into
@@ -56,7 +56,7 @@ constexpr int BK = 64;             // K per stage: 64 x 16-bit = one 128-byte sw
 constexpr int UK = 16;             // K per tcgen05.mma of kind::f16
 constexpr int STAGES = 4;
 constexpr int STATS_TILES = PSTAT_CHUNK_BF16 / BN;  // 16 tiles per statistics chunk
-constexpr int VC = PSTAT_CHUNK_BF16;                // backward vocabulary chunk (columns)
+constexpr int VC = 8192;           // backward vocabulary chunk (columns staged as G / Gt)
 constexpr int M_GROUP = 32;        // M tiles sharing the L2-resident slice of A
 constexpr int THREADS = 192;
 constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
