@@ -3,9 +3,9 @@
 One step is one pass of the hot path over one batch of T = 8192 rows of bf16
 logits N(0, 2^2), labels sampled from each row's softmax, weights N(0, 1) x a
 0/1 mask with 20% zeros: logprob, entropy and bf16 dlogits.  The headline
-step is pstat_forward + pstat_backward (each kernel's bandwidth under
-`kernels`); the same workload through pstat_forward_backward (statistics and
-gradient in one pass over the logits) is timed in the same run under `fused`.
+step is pstat_forward_backward (statistics and gradient in one pass over the
+logits); the same workload through pstat_forward + pstat_backward is timed in
+the same run under `two_call`, with each kernel's bandwidth.
 
 Prints ONE JSON line (rank 0).  `value` is whole-job tokens/s with inputs
 resident in HBM; `e2e` is the same metric through the Python/C-ABI calls with
@@ -323,17 +323,14 @@ def main():
     bwd_gbs = bwd_bytes / (bwd_ms / 1e3) / 1e9
     fwd_gbs = fwd_bytes / (fwd_ms / 1e3) / 1e9
     fused_gbs = fused_bytes / (fused_ms / 1e3) / 1e9
-    dominant = "backward_kernel" if bwd_ms >= fwd_ms else "chunk_stats_kernel"
-    traffic, traffic_rows = traffic_record(dominant)
+    traffic, traffic_rows = traffic_record("fwdbwd_kernel")
     if traffic is not None and traffic_rows:
         traffic = traffic * T / traffic_rows
-    dom_bytes = bwd_bytes if dominant == "backward_kernel" else fwd_bytes
-    dom_gbs = bwd_gbs if dominant == "backward_kernel" else fwd_gbs
-    roof = {"bound": "hbm", "kernel": dominant, "achieved": dom_gbs, "peak": hbm,
-            "unit": "GB/s", "frac": dom_gbs / hbm, "peak_kind": peak_kind, "traffic": traffic,
-            "algorithmic_bytes_per_launch": dom_bytes}
-    ms_step = ms_a / K
-    tok_s = whole_job_rate(T, K, world, ms_a)
+    roof = {"bound": "hbm", "kernel": "fwdbwd_kernel", "achieved": fused_gbs, "peak": hbm,
+            "unit": "GB/s", "frac": fused_gbs / hbm, "peak_kind": peak_kind, "traffic": traffic,
+            "algorithmic_bytes_per_launch": fused_bytes}
+    ms_step = ms_b / K
+    tok_s = whole_job_rate(T, K, world, ms_b)
 
     line = {
         "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": world, "steps": K,
@@ -341,19 +338,19 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"fwdbwd: T={T} rows per GPU x V={V} bf16 logits N(0,2^2), "
                                "sampled labels, weights N(0,1) x mask(20% zero), bf16 dlogits; "
-                               "step = pstat_forward + pstat_backward",
+                               "step = pstat_forward_backward (one pass over the logits)",
                    "global_batch": T * world, "seq_len": None, "parallelism": f"dp{world}",
                    "l2": "inputs larger than L2 (2.49 GB logits per rank)"},
-        "gbs": (fwd_bytes + bwd_bytes) / (ms_step / 1e3) / 1e9,
-        "kernels": {"forward_ms": fwd_ms, "forward_gbs": fwd_gbs, "forward_frac": fwd_gbs / hbm,
-                    "backward_ms": bwd_ms, "backward_gbs": bwd_gbs,
-                    "backward_frac": bwd_gbs / hbm, "active_rows": active_rows},
+        "gbs": fused_gbs,
         "roofline": roof,
-        "gpu_launches": 3 * K,
-        "fused": {"step": "pstat_forward_backward (one pass over the logits)",
-                  "value": whole_job_rate(T, K, world, ms_b), "ms_per_step": ms_b / K,
-                  "kernel_ms": fused_ms, "gbs": fused_gbs, "frac": fused_gbs / hbm,
-                  "algorithmic_bytes_per_launch": fused_bytes, "gpu_launches": K},
+        "gpu_launches": K,
+        "two_call": {"step": "pstat_forward + pstat_backward",
+                     "value": whole_job_rate(T, K, world, ms_a), "ms_per_step": ms_a / K,
+                     "gbs": (fwd_bytes + bwd_bytes) / (ms_a / K / 1e3) / 1e9,
+                     "forward_ms": fwd_ms, "forward_gbs": fwd_gbs, "forward_frac": fwd_gbs / hbm,
+                     "backward_ms": bwd_ms, "backward_gbs": bwd_gbs,
+                     "backward_frac": bwd_gbs / hbm, "active_rows": active_rows,
+                     "gpu_launches": 3 * K},
         "clocks": clocks.summary(),
     }
 
@@ -372,8 +369,7 @@ def main():
             zd.copy_(zh, non_blocking=True)
             yd.copy_(yh, non_blocking=True)
             wd.copy_(wh, non_blocking=True)
-            pstat.forward(zd, yd, -100, None, out=(lp, ent, rs), workspace=ws, dev_error=err)
-            pstat.backward(zd, yd, wd, rs, -100, out=g, dev_error=err)
+            pstat.forward_backward(zd, yd, wd, -100, out=(lp, ent, rs), dlogits=g, dev_error=err)
             outh[0].copy_(lp, non_blocking=True)
             outh[1].copy_(ent, non_blocking=True)
 

@@ -28,8 +28,9 @@
  * restart at every shard start: chunk k of shard s covers columns
  * [b_s + k C, min(b_s + (k+1) C, b_{s+1})), C = PSTAT_CHUNK_BF16 or
  * PSTAT_CHUNK_F32 elements.  Per chunk the kernel forms (m, s, u) with a
- * reduction tree fixed at compile time; chunks are folded in ascending order
- * within a shard and shards in ascending order within the row.  A row's
+ * reduction tree fixed at compile time; within a shard the chunks are folded
+ * by a fixed tree (32 lane-strided ascending partial sums, then an xor
+ * butterfly) and shards in ascending order within the row.  A row's
  * results therefore depend only on its own values, V, the shard bounds and
  * the dtype: they are bit-identical whatever batch the row sits in, at
  * whatever position, and from call to call.  Sharded and unsharded results

@@ -234,35 +234,53 @@ __device__ __forceinline__ void load_chunk_regs(const void* buf, int len, int la
 }
 
 // ---------------------------------------------------------------------------
-// Fixed-order fold of one row's chunk records (see combine_kernel).
+// Fixed-order fold of one row's chunk records, by one warp.
+// A record (m, s, u, dr) holds its sums relative to the reference point
+// m - dr.  Within a shard: M_s = max of its chunk maxima; each chunk moves to
+// M_s with f = e^((m_c - M_s) - dr_c),
+//     S_s = sum_c f s_c,   U_s = sum_c f (u_c + ((m_c - M_s) - dr_c) s_c),
+// the sums taken as: lane L adds the shard's chunks L, L+32, ... (counted
+// from the shard start) in ascending order, then the lanes are added by an
+// xor butterfly.  Across shards, in ascending order, the same with the row
+// maximum M.  Chunks or shards whose maximum is -inf (fully masked) are
+// skipped.  The order depends only on the shard plan, and every lane ends
+// with the same (M, S, U).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float4 fold_row(const float4* c, const ShardPlan& plan) {
+__device__ __forceinline__ float3 fold_row_warp(const float4* rec, const ShardPlan& plan,
+                                                int lane) {
     float M = -INFINITY;
-    for (int g = 0; g < plan.n_chunks; ++g) M = fmaxf(M, c[g].x);
+    for (int c = lane; c < plan.n_chunks; c += 32) M = fmaxf(M, rec[c].x);
+    M = warp_max(M);
     float S = 0.f, U = 0.f;
     if (M > -INFINITY) {
         for (int sh = 0; sh < plan.n_shards; ++sh) {
+            const int c0 = plan.cum[sh], c1 = plan.cum[sh + 1];
             float Ms = -INFINITY;
-            for (int g = plan.cum[sh]; g < plan.cum[sh + 1]; ++g) Ms = fmaxf(Ms, c[g].x);
+            for (int c = c0 + lane; c < c1; c += 32) Ms = fmaxf(Ms, rec[c].x);
+            Ms = warp_max(Ms);
             if (Ms == -INFINITY) continue;
-            float Ss = 0.f, Us = 0.f;
-            for (int g = plan.cum[sh]; g < plan.cum[sh + 1]; ++g) {
-                const float4 r = c[g];
+            float ps = 0.f, pu = 0.f;
+            for (int c = c0 + lane; c < c1; c += 32) {
+                const float4 r = rec[c];
                 if (r.x == -INFINITY) continue;
                 const float dm = (r.x - Ms) - r.w;
                 const float f = expf(dm);
-                Ss = fmaf(r.y, f, Ss);
-                Us = fmaf(f, fmaf(dm, r.y, r.z), Us);
+                ps = fmaf(r.y, f, ps);
+                pu = fmaf(f, fmaf(dm, r.y, r.z), pu);
+            }
+#pragma unroll
+            for (int off = 16; off; off >>= 1) {
+                ps += __shfl_xor_sync(0xFFFFFFFFu, ps, off);
+                pu += __shfl_xor_sync(0xFFFFFFFFu, pu, off);
             }
             const float dM = Ms - M;
             const float f = expf(dM);
-            S = fmaf(Ss, f, S);
-            U = fmaf(f, fmaf(dM, Ss, Us), U);
+            S = fmaf(ps, f, S);
+            U = fmaf(f, fmaf(dM, ps, pu), U);
         }
     }
-    return make_float4(M, S, U, 0.f);
+    return make_float3(M, S, U);
 }
-
 
 // ---------------------------------------------------------------------------
 // Element-wise gradient helpers: 8 elements per 16-byte (bf16) or 32-byte

@@ -12,9 +12,10 @@
 //   pass 2  streams the same chunks again -- now from L2 -- and writes
 //           dlogits with the element-wise arithmetic of the backward kernel.
 // HBM sees 4V bytes per token (read once, write once).  Rows are dealt to
-// CTAs round robin; within a CTA each warp runs pass 1 of a row, then pass 2
-// of the row before it, keeping its 2-slot ring of bulk copies full across
-// passes and rows, so nobody waits for a row's fold.  Every record, fold
+// CTAs round robin; each warp keeps its 2-slot ring of bulk copies full
+// across both passes and across rows.  (Running pass 1 of the next row before
+// pass 2 of the current one hides the fold, but doubles the rows each SM
+// keeps in L2, and pass 2 then misses L2: measured slower.)  Every record, fold
 // and gradient element is computed by the same code as in the two-call path,
 // so the results are bit-identical to pstat_forward + pstat_backward.
 #include <cuda_runtime.h>
@@ -177,42 +178,38 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     }
     fence_mbar_init();
     __syncthreads();
-    // Rotating the chunk assignment keeps every warp in every row only when a
-    // row has at least one chunk per warp; with fewer chunks the assignment is
-    // fixed (warp w owns chunk w of every row) and the other warps leave.  In
-    // both cases each working warp owns a chunk of every row, so it arrives
-    // for every row's fold and reads every row's statistics before the
-    // double-buffered records and row data are reused two rows later.
-    const bool rotate = nc >= kWarps;
-    if (!rotate && warp >= nc) return;
+    // Pass 1 of row k: warp w owns chunks g = w, w + 12, ... .  Pass 2 shifts
+    // the assignment by n_chunks mod 12, so the warps that own one chunk more
+    // than the others in pass 1 are not the ones that do in pass 2 (38 chunks:
+    // warps 0, 1 take 4 + 3 tasks, warps 2, 3 take 3 + 4, the rest 3 + 3).
+    // With at least 12 chunks every warp owns chunks of every row in both
+    // passes, so it arrives for every row's fold and reads every row's
+    // statistics before the double-buffered records and row data are reused
+    // two rows later.  With fewer chunks there is no shift and warps without
+    // a chunk leave.
+    const int shift = nc >= kWarps ? nc % kWarps : 0;
+    if (nc < kWarps && warp >= nc) return;
 
     const int64_t nrows = (T > (int64_t)blockIdx.x) ? (T - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     const uint64_t pol_keep = policy_evict_last();
     const uint64_t pol_once = policy_evict_first();
 
-    // A warp's work is a sequence of segments: for k = 0 .. nrows, pass 1 of
-    // the CTA's row k, then pass 2 of its row k - 1.  So a row's statistics
-    // are folded while the warps already stream the next row, and pass 2
-    // never waits on the slowest warp.  Chunks are dealt round robin over the
-    // concatenated chunk stream of the CTA's rows: warp w owns chunks
-    // g0, g0 + 12, ... of row r, g0 = (w - r nc) mod 12, so the rows' spare
-    // chunks rotate over the warps (when rotating, see above).
+    // A warp's work is the sequence of segments pass 1 of row k, pass 2 of
+    // row k, for the CTA's rows k = 0, 1, ... in order.
     struct Cursor {
         int64_t k;
         int pass, i, cnt, g0;
     };
     auto load_segment = [&](Cursor& c) {
-        const int64_t r = c.k - c.pass;
-        if (r < 0 || r >= nrows) {
+        if (c.k >= nrows) {
             c.cnt = 0;
             return;
         }
-        const int rot = rotate ? (int)((r * nc) % kWarps) : 0;
-        c.g0 = (warp - rot + kWarps) % kWarps;
+        c.g0 = c.pass == 0 ? warp : (warp - shift + kWarps) % kWarps;
         c.cnt = c.g0 < nc ? (nc - c.g0 + kWarps - 1) / kWarps : 0;
     };
     auto settle = [&](Cursor& c) {  // first position at or after c that holds a chunk
-        while (c.k <= nrows) {
+        while (c.k < nrows) {
             load_segment(c);
             if (c.i < c.cnt) return;
             c.i = 0;
@@ -228,7 +225,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         ++c.i;
         settle(c);
     };
-    auto done = [&](const Cursor& c) { return c.k > nrows; };
+    auto done = [&](const Cursor& c) { return c.k >= nrows; };
 
     struct Task {
         int64_t r, t;  // the CTA's row index, token row
@@ -240,7 +237,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     };
     auto task_of = [&](const Cursor& c) {
         Task tk;
-        tk.r = c.k - c.pass;
+        tk.r = c.k;
         tk.g = c.g0 + kWarps * c.i;
         tk.t = blockIdx.x + tk.r * gridDim.x;
         chunk_span(plan, tk.g, tk.start, tk.len);
@@ -326,13 +323,17 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
             if (cc.i == cc.cnt - 1) {
                 // This warp's last chunk of the row: the last warp to get here folds.
                 __syncwarp();
+                int arrived = 0;
                 if (lane == 0) {
                     __threadfence_block();
-                    const int arrived = atomicAdd(&counter[b], 1);
-                    if (arrived == active - 1) {
-                        __threadfence_block();
+                    arrived = atomicAdd(&counter[b], 1);
+                }
+                arrived = __shfl_sync(0xFFFFFFFFu, arrived, 0);
+                if (arrived == active - 1) {
+                    __threadfence_block();
+                    const float3 st = fold_row_warp(records + b * kFbMaxChunks, plan, lane);
+                    if (lane == 0) {
                         counter[b] = 0;
-                        const float4 st = fold_row(records + b * kFbMaxChunks, plan);
                         const float M = st.x, S = st.y, U = st.z;
                         const int64_t t = tk.t;
                         const int64_t y = labels ? labels[t] : ignore_index;

@@ -5,7 +5,7 @@
 
 #include <cstdint>
 
-#include "../../include/pstat.h"
+#include "pstat.h"
 
 namespace pstat {
 

@@ -163,43 +163,24 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 }
 
 // ---------------------------------------------------------------------------
-// K-B: fixed-order combine, one thread per row.
-// A chunk record (m, s, u, dr) holds its sums relative to the reference point
-// m - dr (dr = 0 when the producer shifted by m itself).  Within a shard:
-// M_s = max of its chunk maxima, then its chunks in ascending order are moved
-// to M_s and summed, with f = e^((m_c - M_s) - dr_c):
-//     S_s = sum_c f s_c,   U_s = sum_c f (u_c + ((m_c - M_s) - dr_c) s_c).
-// Across shards: the same with the row maximum M, shards in ascending order.
-// Chunks or shards whose maximum is -inf (fully masked) are skipped.
-// The CTA first copies its rows' records into shared memory with coalesced
-// loads (when they fit), so each thread's sequential fold reads on-chip data.
+// K-B: fixed-order combine, one warp per row (fold_row_warp), then logprob,
+// entropy and (M, ln S) from (M, S, U).
 // ---------------------------------------------------------------------------
-constexpr int kCombineRows = 32;     // rows per CTA
-constexpr int kCombineThreads = 128;
-constexpr int kCombineSmemRecords = 3072;  // 48 KB of float4
+constexpr int kCombineWarps = 8;  // rows per CTA
 
 template <typename E>
-__global__ void __launch_bounds__(kCombineThreads)
+__global__ void __launch_bounds__(kCombineWarps * 32)
     combine_kernel(const float4* __restrict__ cs, const __grid_constant__ ShardPlan plan,
                    const E* __restrict__ logits, int64_t T, int64_t V, int64_t ld,
                    const int64_t* __restrict__ labels, int64_t ignore_index,
                    const float* __restrict__ target, float* __restrict__ logprob,
                    float* __restrict__ entropy, float* __restrict__ rowstats,
                    int* __restrict__ dev_error) {
-    __shared__ float4 stage[kCombineSmemRecords];
-    const int64_t t0 = (int64_t)blockIdx.x * kCombineRows;
-    const int64_t rows = min((int64_t)kCombineRows, T - t0);
-    const int nc = plan.n_chunks;
-    const bool staged = (int64_t)kCombineRows * nc <= kCombineSmemRecords;
-    if (staged) {
-        const int64_t n = rows * nc;
-        const float4* src = cs + t0 * nc;
-        for (int64_t i = threadIdx.x; i < n; i += kCombineThreads) stage[i] = src[i];
-        __syncthreads();
-    }
-    if (threadIdx.x >= rows) return;
-    const int64_t t = t0 + threadIdx.x;
-    const float4 st = fold_row(staged ? stage + (int64_t)threadIdx.x * nc : cs + t * nc, plan);
+    const int lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const float3 st = fold_row_warp(cs + t * plan.n_chunks, plan, lane);
+    if (lane != 0) return;
     const float M = st.x, S = st.y, U = st.z;
     int err = 0;
     float lnS, H, lp;
@@ -366,8 +347,8 @@ cudaError_t launch_combine(const float4* cs, const ShardPlan& plan, const void* 
                            const int64_t* labels, int64_t ignore_index, const float* target,
                            float* logprob, float* entropy, float* rowstats, int* dev_error,
                            cudaStream_t stream) {
-    const int threads = kCombineThreads;
-    const unsigned grid = (unsigned)((T + kCombineRows - 1) / kCombineRows);
+    const int threads = kCombineWarps * 32;
+    const unsigned grid = (unsigned)((T + kCombineWarps - 1) / kCombineWarps);
     if (dt == PSTAT_BF16)
         combine_kernel<uint16_t><<<grid, threads, 0, stream>>>(
             cs, plan, static_cast<const uint16_t*>(logits), T, V, ld, labels, ignore_index,
