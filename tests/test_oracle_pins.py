@@ -303,3 +303,62 @@ def test_lmhead_backward_matches_finite_differences():
             Wm[v, k] -= eps
             fd = (f(h, Wp) - f(h, Wm)) / (2 * eps)
             assert abs(fd - dW[v, k]) <= 1e-7 * max(1.0, abs(dW[v, k]))
+
+
+# ---- loss-side epilogue (oracle/policy.py) ----------------------------------
+from oracle import policy as opol  # noqa: E402
+
+
+def test_diff_metrics_hand_example():
+    pi = np.array([1.0, 2.0, 3.0, 4.0], np.float32)
+    mu = np.array([1.0, 1.5, 5.0, 9.0], np.float32)
+    lab = np.array([0, 1, 2, IGN])          # the last token is ignored
+    m = opol.diff_metrics(pi, mu, lab, IGN)  # d = (0, 0.5, -2)
+    assert m["mean"] == -0.5 and m["abs_mean"] == 2.5 / 3 and m["max"] == 2.0
+    assert m["different"] == 2 / 3
+
+
+def test_diff_metrics_bitwise_and_degenerate():
+    z = np.array([0.0], np.float32)
+    nz = np.array([-0.0], np.float32)
+    m = opol.diff_metrics(z, nz, [0], IGN)   # equal values, different bits
+    assert m["mean"] == 0.0 and m["abs_mean"] == 0.0 and m["different"] == 1.0
+    same = opol.diff_metrics(np.arange(5, dtype=np.float32), np.arange(5, dtype=np.float32),
+                             np.arange(5), IGN)
+    assert same == {"mean": 0.0, "abs_mean": 0.0, "max": 0.0, "different": 0.0}
+    none = opol.diff_metrics(np.ones(3, np.float32), np.zeros(3, np.float32), [IGN] * 3, IGN)
+    assert math.isnan(none["mean"]) and none["max"] == 0.0 and math.isnan(none["different"])
+
+
+@pytest.mark.parametrize("adv,lr,loss,weight", [
+    (1.0, 0.0, -1.0, -1.0),                               # r = 1: unclipped
+    (1.0, 0.5, -1.28, 0.0),                               # r > 1.28, A > 0: clipped, no gradient
+    (-1.0, 0.5, math.exp(0.5), math.exp(0.5)),            # r > 1.28, A < 0: unclipped
+    (1.0, -0.5, -math.exp(-0.5), -math.exp(-0.5)),        # r < 0.8, A > 0: unclipped
+    (-1.0, -0.5, 0.8, 0.0),                               # r < 0.8, A < 0: clipped
+    (2.0, 0.1, -2.0 * math.exp(0.1), -2.0 * math.exp(0.1)),
+])
+def test_clipped_surrogate_cases(adv, lr, loss, weight):
+    l, w = opol.clipped_surrogate([lr], [0.0], [adv], [0], 0.2, 0.28, 1.0, IGN)
+    assert math.isclose(l[0], loss, rel_tol=1e-15, abs_tol=1e-15)
+    assert math.isclose(w[0], weight, rel_tol=1e-15, abs_tol=1e-15)
+    l2, w2 = opol.clipped_surrogate([lr], [0.0], [adv], [IGN], 0.2, 0.28, 1.0, IGN)
+    assert l2[0] == 0.0 and w2[0] == 0.0
+    l3, w3 = opol.clipped_surrogate([lr], [0.0], [adv], [0], 0.2, 0.28, 0.25, IGN)
+    assert math.isclose(l3[0], 0.25 * loss, abs_tol=1e-15) and math.isclose(w3[0], 0.25 * weight, abs_tol=1e-15)
+
+
+def test_clipped_surrogate_weight_is_the_derivative():
+    rng = np.random.default_rng(13)
+    old = rng.normal(-3, 1, 200)
+    pi = old + rng.normal(0, 0.3, 200)
+    adv = rng.normal(0, 1, 200)
+    lab = np.zeros(200, np.int64)
+    _, w = opol.clipped_surrogate(pi, old, adv, lab)
+    h = 1e-6
+    lp, _ = opol.clipped_surrogate(pi + h, old, adv, lab)
+    lm, _ = opol.clipped_surrogate(pi - h, old, adv, lab)
+    fd = (lp - lm) / (2 * h)
+    r = np.exp(pi - old)
+    away = (np.abs(r - 0.8) > 1e-4) & (np.abs(r - 1.28) > 1e-4)  # not at a kink
+    assert np.allclose(fd[away], w[away], rtol=1e-6, atol=1e-9)
