@@ -204,6 +204,41 @@ PSTAT_API int pstat_forward_backward(const void* logits, pstat_dtype dt, int64_t
                                      int64_t ld_out, int* dev_error, pstat_stream_t stream);
 
 /*
+ * Trainer/rollout logprob mismatch metrics, as the torchtitan batch-invariant
+ * GDN README logs them ("Code map": bit_wise/logprob_diff/{mean,abs_mean,max}
+ * and bit_wise/ratio_tokens_different/mean).  Over the tokens whose label is
+ * not ignore_index (all tokens when labels is NULL), d_t = logprob_t -
+ * rollout_logprob_t:
+ *   out_metrics[0] = mean d,  [1] = mean |d|,  [2] = max |d|,
+ *   [3] = fraction of tokens whose float32 bit patterns differ.
+ * With no token counted: [0], [1], [3] are NaN and [2] is 0.  One fixed-order
+ * reduction on the device (double-precision sums): repeated calls give the
+ * same bits.  logprob, rollout_logprob [T] float; out_metrics device float[4].
+ */
+PSTAT_API int pstat_logprob_diff_metrics(const float* logprob, const float* rollout_logprob,
+                                         const int64_t* labels, int64_t ignore_index, int64_t T,
+                                         float* out_metrics, pstat_stream_t stream);
+
+/*
+ * Clipped-ratio policy surrogate (the DAPO recipes of the same README use
+ * eps_low = 0.2, eps_high = 0.28), per token, with r_t = exp(logprob_t -
+ * old_logprob_t):
+ *   out_loss_t   = -scale min(r_t A_t, clip(r_t, 1 - eps_low, 1 + eps_high) A_t)
+ *   out_weight_t = d out_loss_t / d logprob_t
+ *                = -scale A_t r_t if the unclipped term is the minimum (or
+ *                  ties), else 0 (the clipped term does not depend on logprob).
+ * Ignored tokens get loss 0 and weight 0.  out_weight is what pstat_backward
+ * and pstat_forward_backward take as `weights` to give the loss's gradient
+ * with respect to the logits.  All arrays [T] float (out_loss may be NULL);
+ * 0 <= eps_low < 1, eps_high >= 0.
+ */
+PSTAT_API int pstat_clipped_surrogate(const float* logprob, const float* old_logprob,
+                                      const float* advantages, const int64_t* labels,
+                                      int64_t ignore_index, int64_t T, float eps_low,
+                                      float eps_high, float scale, float* out_loss,
+                                      float* out_weight, pstat_stream_t stream);
+
+/*
  * Workspace bytes for the fused lm_head entry points (T tokens, V vocab
  * rows, hidden size d).
  */

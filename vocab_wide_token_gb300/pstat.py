@@ -43,6 +43,11 @@ _lib.pstat_backward.restype = _i32
 _lib.pstat_forward_backward.argtypes = [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _i32,
                                         _vp, _vp, _vp, _vp, _i32, _i64, _vp, _vp]
 _lib.pstat_forward_backward.restype = _i32
+_lib.pstat_logprob_diff_metrics.argtypes = [_vp, _vp, _vp, _i64, _i64, _vp, _vp]
+_lib.pstat_logprob_diff_metrics.restype = _i32
+_lib.pstat_clipped_surrogate.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_float,
+                                         ctypes.c_float, ctypes.c_float, _vp, _vp, _vp]
+_lib.pstat_clipped_surrogate.restype = _i32
 _lib.pstat_lmhead_workspace_size.argtypes = [_i64, _i64, _i64, ctypes.POINTER(_sz)]
 _lib.pstat_lmhead_workspace_size.restype = _i32
 _lib.pstat_lmhead_fused.argtypes = [_vp, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _vp,
@@ -257,6 +262,46 @@ def forward_backward(logits: torch.Tensor, labels: torch.Tensor | None,
                                        _ptr(dev_error), _stream(dev)),
            "pstat_forward_backward")
     return lp, ent, rs, dlogits
+
+
+def _f32_vec(x, T, dev, name):
+    if x.dtype != torch.float32 or x.shape != (T,) or x.device != dev:
+        raise ValueError(f"{name} must be float32 [T] on the same device")
+    return x.contiguous()
+
+
+def logprob_diff_metrics(logprob, rollout_logprob, labels=None, ignore_index: int = -100):
+    """(mean d, mean |d|, max |d|, fraction of bitwise-different tokens) over
+    non-ignored tokens, d = logprob - rollout_logprob; a float32 [4] tensor."""
+    T = logprob.shape[0]
+    dev = logprob.device
+    a = _f32_vec(logprob, T, dev, "logprob")
+    b = _f32_vec(rollout_logprob, T, dev, "rollout_logprob")
+    lab = _labels(labels, T, dev)
+    out = torch.empty(4, dtype=torch.float32, device=dev)
+    _check(_lib.pstat_logprob_diff_metrics(_ptr(a), _ptr(b), _ptr(lab), int(ignore_index), T,
+                                           _ptr(out), _stream(dev)),
+           "pstat_logprob_diff_metrics")
+    return out
+
+
+def clipped_surrogate(logprob, old_logprob, advantages, labels=None, eps_low: float = 0.2,
+                      eps_high: float = 0.28, scale: float = 1.0, ignore_index: int = -100):
+    """Per-token clipped-ratio loss and its derivative d loss / d logprob
+    (the backward's per-token weights).  Returns (loss [T], weight [T])."""
+    T = logprob.shape[0]
+    dev = logprob.device
+    a = _f32_vec(logprob, T, dev, "logprob")
+    b = _f32_vec(old_logprob, T, dev, "old_logprob")
+    c = _f32_vec(advantages, T, dev, "advantages")
+    lab = _labels(labels, T, dev)
+    loss = torch.empty(T, dtype=torch.float32, device=dev)
+    weight = torch.empty(T, dtype=torch.float32, device=dev)
+    _check(_lib.pstat_clipped_surrogate(_ptr(a), _ptr(b), _ptr(c), _ptr(lab), int(ignore_index), T,
+                                        float(eps_low), float(eps_high), float(scale), _ptr(loss),
+                                        _ptr(weight), _stream(dev)),
+           "pstat_clipped_surrogate")
+    return loss, weight
 
 
 def lmhead_workspace_size(T: int, V: int, d: int) -> int:
