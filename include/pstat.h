@@ -204,6 +204,24 @@ PSTAT_API int pstat_forward_backward(const void* logits, pstat_dtype dt, int64_t
                                      int64_t ld_out, int* dev_error, pstat_stream_t stream);
 
 /*
+ * The full log-softmax log p_tv = z_tv - M_t - ln S_t as a [T, V] tensor, in
+ * one read and one write pass over the logits, from the same row statistics
+ * as the other entry points (so it is batch-invariant too: a row's output
+ * bits do not depend on the batch).  The BI log_softmax of the batch-
+ * invariant GDN README's kernel list, for callers that need every column.
+ *   rowstats  [T, 2] (M, ln S) from pstat_forward with the same shard bounds,
+ *             or NULL to compute them first (needs the workspace).
+ *   out       [T, ld_out] of out_dt (bf16 rounds to nearest even); -inf
+ *             logits give -inf, rows with no finite logit give NaN and set
+ *             PSTAT_DEV_EMPTY_ROW.
+ */
+PSTAT_API int pstat_log_softmax(const void* logits, pstat_dtype dt, int64_t T, int64_t V,
+                                int64_t ld, const float* rowstats, const int64_t* shard_bounds,
+                                int n_shards, void* out, pstat_dtype out_dt, int64_t ld_out,
+                                void* workspace, size_t ws_bytes, int* dev_error,
+                                pstat_stream_t stream);
+
+/*
  * Trainer/rollout logprob mismatch metrics, as the torchtitan batch-invariant
  * GDN README logs them ("Code map": bit_wise/logprob_diff/{mean,abs_mean,max}
  * and bit_wise/ratio_tokens_different/mean).  Over the tokens whose label is

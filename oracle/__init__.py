@@ -135,6 +135,18 @@ def backward(z, labels, weights=None, ignore_index=-100):
     return out
 
 
+def log_softmax(z):
+    """log softmax of every row, float64 [T, V]: z - (M + ln S) with (M, ln S)
+    from ``forward`` (the log-partition of the plain definition)."""
+    zz, code, ld = _as_logits(z)
+    st = forward(zz, None)
+    if code == BF16:
+        z64 = bf16_to_f64(zz)
+    else:
+        z64 = zz.astype(np.float64)
+    return z64 - (st["M"] + st["logS"])[:, None]
+
+
 def sharded(z, labels, bounds, ignore_index=-100):
     """Shard-local (m, s, u) [T, n_shards, 3] and the combined logprob/entropy."""
     z, code, ld = _as_logits(z)

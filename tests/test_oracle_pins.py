@@ -362,3 +362,15 @@ def test_clipped_surrogate_weight_is_the_derivative():
     r = np.exp(pi - old)
     away = (np.abs(r - 0.8) > 1e-4) & (np.abs(r - 1.28) > 1e-4)  # not at a kink
     assert np.allclose(fd[away], w[away], rtol=1e-6, atol=1e-9)
+
+
+def test_log_softmax_matches_scipy_and_normalises():
+    rng = np.random.default_rng(21)
+    z = rng.standard_normal((5, 3001)) * 3
+    z[2, :100] = -np.inf
+    ls = oracle.log_softmax(z)
+    ref = scipy.special.log_softmax(z, axis=1)
+    fin = np.isfinite(ref)
+    assert np.allclose(ls[fin], ref[fin], rtol=0, atol=1e-12)
+    assert np.all(np.isneginf(ls[~fin]))
+    assert np.allclose(np.exp(ls).sum(axis=1), 1.0, rtol=0, atol=1e-12)

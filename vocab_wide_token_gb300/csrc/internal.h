@@ -58,4 +58,8 @@ cudaError_t launch_backward(const void* logits, pstat_dtype dt, int64_t T, int64
                             pstat_dtype out_dt, int64_t ld_out, int* dev_error,
                             const DeviceInfo& dev, cudaStream_t stream);
 
+cudaError_t launch_logsoftmax(const void* logits, pstat_dtype dt, int64_t T, int64_t V, int64_t ld,
+                              const float* rowstats, void* out, pstat_dtype out_dt, int64_t ld_out,
+                              int* dev_error, cudaStream_t stream);
+
 }  // namespace pstat

@@ -195,4 +195,46 @@ int pstat_backward(const void* logits, pstat_dtype dt, int64_t T, int64_t V, int
     return PSTAT_OK;
 }
 
+int pstat_log_softmax(const void* logits, pstat_dtype dt, int64_t T, int64_t V, int64_t ld,
+                      const float* rowstats, const int64_t* shard_bounds, int n_shards,
+                      void* out, pstat_dtype out_dt, int64_t ld_out, void* workspace,
+                      size_t ws_bytes, int* dev_error, pstat_stream_t stream) {
+    if (!valid_dtype(dt) || !valid_dtype(out_dt)) return PSTAT_ERR_DTYPE;
+    if (T < 0 || V < 1 || ld < V || ld_out < V) return PSTAT_ERR_SHAPE;
+    ShardPlan plan;
+    int rc = make_plan(V, chunk_for(dt), shard_bounds, n_shards, &plan);
+    if (rc != PSTAT_OK) return rc;
+    if (T == 0) return PSTAT_OK;
+    if (!logits || !out) return PSTAT_ERR_NULLPTR;
+    if ((reinterpret_cast<uintptr_t>(logits) % elem_size(dt)) != 0 ||
+        (reinterpret_cast<uintptr_t>(out) % elem_size(out_dt)) != 0 ||
+        (rowstats && (reinterpret_cast<uintptr_t>(rowstats) & 7u)))
+        return PSTAT_ERR_ALIGN;
+    const StatsWorkspace wl = stats_workspace_layout(T, plan);
+    if (rowstats == nullptr) {
+        if (!workspace || ws_bytes < wl.total) return PSTAT_ERR_WORKSPACE;
+        if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return PSTAT_ERR_ALIGN;
+    }
+    DeviceInfo dev;
+    rc = device_info(&dev);
+    if (rc != PSTAT_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const float* rs = rowstats;
+    if (rs == nullptr) {
+        char* ws = static_cast<char*>(workspace);
+        float4* cs = reinterpret_cast<float4*>(ws + wl.chunk_stats_off);
+        float* rws = reinterpret_cast<float*>(ws + wl.rowstats_off);
+        if (launch_chunk_stats(logits, dt, T, ld, plan, cs, dev_error, dev, st) != cudaSuccess)
+            return PSTAT_ERR_CUDA;
+        if (launch_combine(cs, plan, logits, dt, T, V, ld, nullptr, -1, nullptr, nullptr, nullptr,
+                           rws, dev_error, st) != cudaSuccess)
+            return PSTAT_ERR_CUDA;
+        rs = rws;
+    }
+    if (launch_logsoftmax(logits, dt, T, V, ld, rs, out, out_dt, ld_out, dev_error, st) !=
+        cudaSuccess)
+        return PSTAT_ERR_CUDA;
+    return PSTAT_OK;
+}
+
 }  // extern "C"

@@ -307,6 +307,56 @@ __global__ void __launch_bounds__(kBwdThreads)
 }
 
 // ---------------------------------------------------------------------------
+// Full log-softmax from the row statistics: out = (z - M) - ln S, element-
+// wise, in the layout and with the streaming scheme of the backward kernel.
+// Rows whose statistics are undefined (every logit -inf) are written as NaN.
+// ---------------------------------------------------------------------------
+template <typename Ein, typename Eout>
+__global__ void __launch_bounds__(kBwdThreads)
+    logsoftmax_kernel(const Ein* __restrict__ logits, int64_t V, int64_t ld,
+                      const float2* __restrict__ rowstats, Eout* __restrict__ out, int64_t ld_out,
+                      int segs, int* __restrict__ dev_error) {
+    const int64_t t = blockIdx.x / segs;
+    const int seg = (int)(blockIdx.x - t * segs);
+    const int64_t nv_row = V >> 3;
+    const int64_t c0 = (nv_row * seg / segs) << 3;
+    const int64_t c1 = (seg == segs - 1) ? V : ((nv_row * (seg + 1) / segs) << 3);
+    const Ein* zin = logits + t * ld;
+    Eout* zout = out + t * ld_out;
+    const float2 rs = rowstats[t];
+    const bool defined = (rs.x > -INFINITY) && (rs.y == rs.y);
+    if (!defined && seg == 0 && threadIdx.x == 0 && dev_error) atomicOr(dev_error, PSTAT_DEV_EMPTY_ROW);
+    const float M = defined ? rs.x : NAN, lnS = defined ? rs.y : NAN;
+    const uint64_t negM = f2_pack(-M, -M), nlnS = f2_pack(-lnS, -lnS);
+    const bool vec_ok = ((reinterpret_cast<uintptr_t>(zin + c0) & 15u) == 0) &&
+                        ((reinterpret_cast<uintptr_t>(zout + c0) & 15u) == 0);
+    const int64_t nv = vec_ok ? (c1 - c0) >> 3 : 0;
+    for (int64_t base = 0; base < nv; base += (int64_t)kBwdThreads * kBwdUnroll) {
+        float x[kBwdUnroll][8];
+        int64_t col[kBwdUnroll];
+#pragma unroll
+        for (int k = 0; k < kBwdUnroll; ++k) {
+            const int64_t i = base + (int64_t)k * kBwdThreads + threadIdx.x;
+            col[k] = (i < nv) ? c0 + (i << 3) : -1;
+            if (col[k] >= 0) Load8<Ein>::run(zin + col[k], x[k]);
+        }
+#pragma unroll
+        for (int k = 0; k < kBwdUnroll; ++k) {
+            if (col[k] < 0) continue;
+            float o[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint64_t d = f2_add(f2_pack(x[k][2 * i], x[k][2 * i + 1]), negM);
+                f2_unpack(f2_add(d, nlnS), o[2 * i], o[2 * i + 1]);
+            }
+            Store8<Eout>::run(zout + col[k], o);
+        }
+    }
+    for (int64_t c = c0 + (nv << 3) + threadIdx.x; c < c1; c += kBwdThreads)
+        zout[c] = out_cast((Elem<Ein>::to_float(zin[c]) - M) - lnS, zout);
+}
+
+// ---------------------------------------------------------------------------
 // Launchers.
 // ---------------------------------------------------------------------------
 template <typename E>
@@ -394,6 +444,39 @@ cudaError_t launch_backward(const void* logits, pstat_dtype dt, int64_t T, int64
         launch_backward_t(static_cast<const float*>(logits), T, V, ld, labels, ignore_index,
                           weights, rowstats, static_cast<float*>(out), ld_out, dev_error, dev,
                           stream);
+    return cudaGetLastError();
+}
+
+}  // namespace pstat
+
+namespace pstat {
+
+template <typename Ein, typename Eout>
+static void launch_logsoftmax_t(const Ein* logits, int64_t T, int64_t V, int64_t ld,
+                                const float* rowstats, Eout* out, int64_t ld_out, int* dev_error,
+                                cudaStream_t stream) {
+    int64_t segs = V / 32768;
+    if (segs < 1) segs = 1;
+    if (segs > 64) segs = 64;
+    logsoftmax_kernel<Ein, Eout><<<(unsigned)(T * segs), kBwdThreads, 0, stream>>>(
+        logits, V, ld, reinterpret_cast<const float2*>(rowstats), out, ld_out, (int)segs, dev_error);
+}
+
+cudaError_t launch_logsoftmax(const void* logits, pstat_dtype dt, int64_t T, int64_t V, int64_t ld,
+                              const float* rowstats, void* out, pstat_dtype out_dt, int64_t ld_out,
+                              int* dev_error, cudaStream_t stream) {
+    if (dt == PSTAT_BF16 && out_dt == PSTAT_BF16)
+        launch_logsoftmax_t(static_cast<const uint16_t*>(logits), T, V, ld, rowstats,
+                            static_cast<uint16_t*>(out), ld_out, dev_error, stream);
+    else if (dt == PSTAT_BF16)
+        launch_logsoftmax_t(static_cast<const uint16_t*>(logits), T, V, ld, rowstats,
+                            static_cast<float*>(out), ld_out, dev_error, stream);
+    else if (out_dt == PSTAT_BF16)
+        launch_logsoftmax_t(static_cast<const float*>(logits), T, V, ld, rowstats,
+                            static_cast<uint16_t*>(out), ld_out, dev_error, stream);
+    else
+        launch_logsoftmax_t(static_cast<const float*>(logits), T, V, ld, rowstats,
+                            static_cast<float*>(out), ld_out, dev_error, stream);
     return cudaGetLastError();
 }
 

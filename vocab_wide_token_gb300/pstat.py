@@ -43,6 +43,9 @@ _lib.pstat_backward.restype = _i32
 _lib.pstat_forward_backward.argtypes = [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _i32,
                                         _vp, _vp, _vp, _vp, _i32, _i64, _vp, _vp]
 _lib.pstat_forward_backward.restype = _i32
+_lib.pstat_log_softmax.argtypes = [_vp, _i32, _i64, _i64, _i64, _vp, _vp, _i32, _vp, _i32, _i64,
+                                   _vp, _sz, _vp, _vp]
+_lib.pstat_log_softmax.restype = _i32
 _lib.pstat_logprob_diff_metrics.argtypes = [_vp, _vp, _vp, _i64, _i64, _vp, _vp]
 _lib.pstat_logprob_diff_metrics.restype = _i32
 _lib.pstat_clipped_surrogate.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_float,
@@ -262,6 +265,31 @@ def forward_backward(logits: torch.Tensor, labels: torch.Tensor | None,
                                        _ptr(dev_error), _stream(dev)),
            "pstat_forward_backward")
     return lp, ent, rs, dlogits
+
+
+def log_softmax(logits: torch.Tensor, rowstats: torch.Tensor | None = None, shard_bounds=None,
+                out_dtype: torch.dtype | None = None, *, out=None, workspace=None,
+                dev_error=None):
+    """Every column's log-probability, [T, V] of `out_dtype` (default: the
+    logits dtype), from (M, ln S) -- computed first when rowstats is None."""
+    T, V, ld = _rows(logits)
+    dev = logits.device
+    out_dtype = out_dtype or logits.dtype
+    if out is None:
+        out = torch.empty(T, V, dtype=out_dtype, device=dev)
+    ld_out = out.stride(0) if T > 1 else V
+    arr, ns = _bounds(shard_bounds, V)
+    ws_ptr, ws_n = None, 0
+    if rowstats is None:
+        need = workspace_size(T, V, logits.dtype, shard_bounds)
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        ws_ptr, ws_n = _ptr(workspace), workspace.numel()
+    _check(_lib.pstat_log_softmax(_ptr(logits), _dtype_code(logits), T, V, ld, _ptr(rowstats), arr,
+                                  ns, _ptr(out), _dtype_code(out), ld_out, ws_ptr, ws_n,
+                                  _ptr(dev_error), _stream(dev)),
+           "pstat_log_softmax")
+    return out
 
 
 def _f32_vec(x, T, dev, name):
