@@ -93,10 +93,12 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
     return r;
 }
 
+// Maximum over the 32 lanes of a converged warp in one reduction (NaN inputs
+// ignored, as fmaxf does; exact, so the order of the lanes does not matter).
 __device__ __forceinline__ float warp_max(float m) {
-#pragma unroll
-    for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
-    return m;
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(m));
+    return r;
 }
 
 __device__ __forceinline__ float hsum2(uint64_t p) {

@@ -32,6 +32,10 @@ namespace pstat {
 namespace {
 
 constexpr int kFbMaxChunks = 256;  // chunk records per row held in shared memory
+// Warps per CTA.  13 rather than the 12 of the chunk-statistics kernel: a
+// 38-chunk row then splits 3 / 3 / ... / 2 over the warps instead of
+// 4 / 4 / 3 / ... / 3, and every row waits for its slowest warp.
+constexpr int kFbWarps = 13;
 
 struct RowInfo {
     float M, log2S, w;
@@ -40,8 +44,8 @@ struct RowInfo {
     long long pad;
 };
 
-constexpr size_t kRingBytes = (size_t)kWarps * kStages * kSlotBytes;
-constexpr size_t kBarBytes = (size_t)kWarps * kStages * sizeof(uint64_t);
+constexpr size_t kRingBytes = (size_t)kFbWarps * kStages * kSlotBytes;
+constexpr size_t kBarBytes = (size_t)kFbWarps * kStages * sizeof(uint64_t);
 constexpr size_t kRecOff = kRingBytes + kBarBytes;
 constexpr size_t kInfoOff = kRecOff + 2 * kFbMaxChunks * sizeof(float4);
 constexpr size_t kReadyOff = kInfoOff + 2 * sizeof(RowInfo);
@@ -147,7 +151,7 @@ __device__ __forceinline__ void unpack_vec<float>(const uint4& v, float (&x)[4])
 }
 
 template <typename Ein, typename Eout>
-__global__ void __launch_bounds__(kWarps * 32, 1)
+__global__ void __launch_bounds__(kFbWarps * 32, 1)
     fwdbwd_kernel(const Ein* __restrict__ logits, int64_t T, int64_t V, int64_t ld,
                   const __grid_constant__ ShardPlan plan, const int64_t* __restrict__ labels,
                   int64_t ignore_index, const float* __restrict__ weights,
@@ -166,7 +170,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     int* counter = reinterpret_cast<int*>(smem + kCountOff);
 
     const int nc = plan.n_chunks;
-    const int active = nc < kWarps ? nc : kWarps;  // warps that own chunks of any one row
+    const int active = nc < kFbWarps ? nc : kFbWarps;  // warps that own chunks of any one row
     if (lane == 0) {
         for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
     }
@@ -178,17 +182,17 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     }
     fence_mbar_init();
     __syncthreads();
-    // Pass 1 of row k: warp w owns chunks g = w, w + 12, ... .  Pass 2 shifts
-    // the assignment by n_chunks mod 12, so the warps that own one chunk more
-    // than the others in pass 1 are not the ones that do in pass 2 (38 chunks:
-    // warps 0, 1 take 4 + 3 tasks, warps 2, 3 take 3 + 4, the rest 3 + 3).
-    // With at least 12 chunks every warp owns chunks of every row in both
+    // Pass 1 of row k: warp w owns chunks g = w, w + 13, ... .  Pass 2 shifts
+    // the assignment by n_chunks mod 13, so the warps that own one chunk more
+    // than the others in pass 1 are not all the ones that do in pass 2 (38
+    // chunks: warps 0..11 take 3 in pass 1, warp 12 takes 2; in pass 2 warp
+    // 11 takes 2).  With at least 13 chunks every warp owns chunks of every row in both
     // passes, so it arrives for every row's fold and reads every row's
     // statistics before the double-buffered records and row data are reused
     // two rows later.  With fewer chunks there is no shift and warps without
     // a chunk leave.
-    const int shift = nc >= kWarps ? nc % kWarps : 0;
-    if (nc < kWarps && warp >= nc) return;
+    const int shift = nc >= kFbWarps ? nc % kFbWarps : 0;
+    if (nc < kFbWarps && warp >= nc) return;
 
     const int64_t nrows = (T > (int64_t)blockIdx.x) ? (T - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     const uint64_t pol_keep = policy_evict_last();
@@ -205,8 +209,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
             c.cnt = 0;
             return;
         }
-        c.g0 = c.pass == 0 ? warp : (warp - shift + kWarps) % kWarps;
-        c.cnt = c.g0 < nc ? (nc - c.g0 + kWarps - 1) / kWarps : 0;
+        c.g0 = c.pass == 0 ? warp : (warp - shift + kFbWarps) % kFbWarps;
+        c.cnt = c.g0 < nc ? (nc - c.g0 + kFbWarps - 1) / kFbWarps : 0;
     };
     auto settle = [&](Cursor& c) {  // first position at or after c that holds a chunk
         while (c.k < nrows) {
@@ -238,7 +242,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     auto task_of = [&](const Cursor& c) {
         Task tk;
         tk.r = c.k;
-        tk.g = c.g0 + kWarps * c.i;
+        tk.g = c.g0 + kFbWarps * c.i;
         tk.t = blockIdx.x + tk.r * gridDim.x;
         chunk_span(plan, tk.g, tk.start, tk.len);
         tk.src = logits + tk.t * ld + tk.start;
@@ -466,7 +470,7 @@ cudaError_t launch_fused_t(const Ein* logits, int64_t T, int64_t V, int64_t ld,
         if (d < 64) configured[d].store(true, std::memory_order_release);
     }
     const int64_t grid = T < dev.sm_count ? T : dev.sm_count;
-    fwdbwd_kernel<Ein, Eout><<<(unsigned)grid, kWarps * 32, kFusedSmem, stream>>>(
+    fwdbwd_kernel<Ein, Eout><<<(unsigned)grid, kFbWarps * 32, kFusedSmem, stream>>>(
         logits, T, V, ld, plan, labels, ignore_index, weights, logprob, entropy, rowstats, out,
         ld_out, dev_error);
     return cudaGetLastError();
