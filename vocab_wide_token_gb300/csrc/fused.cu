@@ -36,6 +36,7 @@ constexpr int kFbMaxChunks = 256;  // chunk records per row held in shared memor
 // 38-chunk row then splits 3 / 3 / ... / 2 over the warps instead of
 // 4 / 4 / 3 / ... / 3, and every row waits for its slowest warp.
 constexpr int kFbWarps = 13;
+constexpr int kFbStages = 2;  // bulk-copy slots per warp
 
 struct RowInfo {
     float M, log2S, w;
@@ -44,13 +45,15 @@ struct RowInfo {
     long long pad;
 };
 
-constexpr size_t kRingBytes = (size_t)kFbWarps * kStages * kSlotBytes;
-constexpr size_t kBarBytes = (size_t)kFbWarps * kStages * sizeof(uint64_t);
-constexpr size_t kRecOff = kRingBytes + kBarBytes;
+constexpr size_t kRingBytes = (size_t)kFbWarps * kFbStages * kSlotBytes;
+constexpr size_t kBarBytes = (size_t)kFbWarps * kFbStages * sizeof(uint64_t);
+constexpr size_t kRecOff = (kRingBytes + kBarBytes + 15) / 16 * 16;  // float4 records
 constexpr size_t kInfoOff = kRecOff + 2 * kFbMaxChunks * sizeof(float4);
 constexpr size_t kReadyOff = kInfoOff + 2 * sizeof(RowInfo);
 constexpr size_t kCountOff = kReadyOff + 2 * sizeof(uint64_t);
 constexpr size_t kFusedSmem = kCountOff + 2 * sizeof(int);
+static_assert(kRingBytes % 16 == 0 && kRecOff % 16 == 0, "slots and records: 16-byte aligned");
+static_assert(kInfoOff % 8 == 0 && kReadyOff % 8 == 0, "RowInfo and mbarriers: 8-byte aligned");
 
 template <typename E>
 struct OutVec;
@@ -162,8 +165,8 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    uint8_t* slots = smem + (size_t)warp * kStages * kSlotBytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRingBytes) + warp * kStages;
+    uint8_t* slots = smem + (size_t)warp * kFbStages * kSlotBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRingBytes) + warp * kFbStages;
     float4* records = reinterpret_cast<float4*>(smem + kRecOff);
     RowInfo* info = reinterpret_cast<RowInfo*>(smem + kInfoOff);
     uint64_t* ready = reinterpret_cast<uint64_t*>(smem + kReadyOff);
@@ -172,7 +175,7 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
     const int nc = plan.n_chunks;
     const int active = nc < kFbWarps ? nc : kFbWarps;  // warps that own chunks of any one row
     if (lane == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+        for (int s = 0; s < kFbStages; ++s) mbar_init(&bars[s], 1);
     }
     if (threadIdx.x == 0) {
         mbar_init(&ready[0], 1);
@@ -253,7 +256,7 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
     auto issue = [&](const Cursor& c, int64_t pos) {
         const Task tk = task_of(c);
         if (tk.bulk && lane == 0) {
-            const int slot = (int)(pos % kStages);
+            const int slot = (int)(pos % kFbStages);
             const uint32_t bytes = (uint32_t)tk.len * (uint32_t)sizeof(Ein);
             // pass 1: the row is read again by pass 2, so keep it in L2
             mbar_arrive_expect_tx(&bars[slot], bytes);
@@ -265,7 +268,7 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
     Cursor ci = {0, 0, 0, 0, 0};  // next position to issue
     settle(ci);
     int64_t pi = 0;
-    for (int s = 0; s < kStages && !done(ci); ++s, ++pi) {
+    for (int s = 0; s < kFbStages && !done(ci); ++s, ++pi) {
         issue(ci, pi);
         advance(ci);
     }
@@ -279,7 +282,7 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
     while (!done(cc)) {
         const Task tk = task_of(cc);
         const int b = (int)(tk.r & 1);
-        const int slot = (int)(pc % kStages);
+        const int slot = (int)(pc % kFbStages);
         Ein* buf = reinterpret_cast<Ein*>(slots + (size_t)slot * kSlotBytes);
         const int len = tk.len;
         const int64_t start = tk.start;
@@ -444,7 +447,7 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
         // Drain copies still in flight into this CTA's shared memory before leaving.
         for (int64_t p = pc; p < pi; ++p) {
             if (task_of(cc).bulk) {
-                const int slot = (int)(p % kStages);
+                const int slot = (int)(p % kFbStages);
                 mbar_wait_bounded(&bars[slot], (phase >> slot) & 1u, kWaitLimitNs);
                 phase ^= 1u << slot;
             }
