@@ -42,7 +42,8 @@ struct RowInfo {
     float M, log2S, w;
     int mode;  // 0: all-zero row, 1: NaN row, 2: compute
     long long y;
-    long long pad;
+    float zy;  // the label's logit (mode 2)
+    int pad;
 };
 
 constexpr size_t kRingBytes = (size_t)kFbWarps * kFbStages * kSlotBytes;
@@ -51,7 +52,12 @@ constexpr size_t kRecOff = (kRingBytes + kBarBytes + 15) / 16 * 16;  // float4 r
 constexpr size_t kInfoOff = kRecOff + 2 * kFbMaxChunks * sizeof(float4);
 constexpr size_t kReadyOff = kInfoOff + 2 * sizeof(RowInfo);
 constexpr size_t kCountOff = kReadyOff + 2 * sizeof(uint64_t);
-constexpr size_t kFusedSmem = kCountOff + 2 * sizeof(int);
+// Labels and weights of the CTA's first kFbRowCache rows, loaded once at the
+// start so that the fold finds them in shared memory.
+constexpr int kFbRowCache = 384;
+constexpr size_t kLabOff = (kCountOff + 2 * sizeof(int) + 7) / 8 * 8;
+constexpr size_t kWtOff = kLabOff + kFbRowCache * sizeof(int64_t);
+constexpr size_t kFusedSmem = kWtOff + kFbRowCache * sizeof(float);
 static_assert(kRingBytes % 16 == 0 && kRecOff % 16 == 0, "slots and records: 16-byte aligned");
 static_assert(kInfoOff % 8 == 0 && kReadyOff % 8 == 0, "RowInfo and mbarriers: 8-byte aligned");
 
@@ -171,6 +177,8 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
     RowInfo* info = reinterpret_cast<RowInfo*>(smem + kInfoOff);
     uint64_t* ready = reinterpret_cast<uint64_t*>(smem + kReadyOff);
     int* counter = reinterpret_cast<int*>(smem + kCountOff);
+    int64_t* lab_s = reinterpret_cast<int64_t*>(smem + kLabOff);
+    float* wt_s = reinterpret_cast<float*>(smem + kWtOff);
 
     const int nc = plan.n_chunks;
     const int active = nc < kFbWarps ? nc : kFbWarps;  // warps that own chunks of any one row
@@ -182,6 +190,12 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
         mbar_init(&ready[1], 1);
         counter[0] = 0;
         counter[1] = 0;
+    }
+    const int64_t nrows = (T > (int64_t)blockIdx.x) ? (T - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    for (int64_t r = threadIdx.x; r < nrows && r < kFbRowCache; r += blockDim.x) {
+        const int64_t t = blockIdx.x + r * gridDim.x;
+        lab_s[r] = labels ? labels[t] : ignore_index;
+        wt_s[r] = weights ? weights[t] : 1.f;
     }
     fence_mbar_init();
     __syncthreads();
@@ -197,7 +211,6 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
     const int shift = nc >= kFbWarps ? nc % kFbWarps : 0;
     if (nc < kFbWarps && warp >= nc) return;
 
-    const int64_t nrows = (T > (int64_t)blockIdx.x) ? (T - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     const uint64_t pol_keep = policy_evict_last();
     const uint64_t pol_once = policy_evict_first();
 
@@ -278,7 +291,7 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
     int64_t pc = 0;
     uint32_t phase = 0;  // parity bit per ring slot
     bool failed = false;
-    RowInfo ri = {0.f, 0.f, 0.f, 0, 0, 0};
+    RowInfo ri = {0.f, 0.f, 0.f, 0, 0, 0.f, 0};
     while (!done(cc)) {
         const Task tk = task_of(cc);
         const int b = (int)(tk.r & 1);
@@ -338,13 +351,19 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
                 arrived = __shfl_sync(0xFFFFFFFFu, arrived, 0);
                 if (arrived == active - 1) {
                     __threadfence_block();
+                    // Label, weight and z_y first: the z_y load then runs
+                    // under the fold's arithmetic.
+                    const int64_t t = tk.t;
+                    const bool cached = tk.r < kFbRowCache;
+                    const int64_t y = cached ? lab_s[tk.r] : (labels ? labels[t] : ignore_index);
+                    const float w = cached ? wt_s[tk.r] : (weights ? weights[t] : 1.f);
+                    const bool y_in = y != ignore_index && y >= 0 && y < V;
+                    float zy = 0.f;
+                    if (lane == 0 && y_in) zy = Elem<Ein>::to_float(logits[t * ld + y]);
                     const float3 st = fold_row_warp(records + b * kFbMaxChunks, plan, lane);
                     if (lane == 0) {
                         counter[b] = 0;
                         const float M = st.x, S = st.y, U = st.z;
-                        const int64_t t = tk.t;
-                        const int64_t y = labels ? labels[t] : ignore_index;
-                        const float w = weights ? weights[t] : 1.f;
                         int err = 0;
                         float lnS, H, lp;
                         RowInfo nr;
@@ -364,7 +383,6 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
                                 lp = NAN;
                                 H = NAN;
                             } else {
-                                const float zy = Elem<Ein>::to_float(logits[t * ld + y]);
                                 lp = (zy - M) - lnS;
                             }
                         }
@@ -377,6 +395,7 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
                         nr.M = M;
                         nr.log2S = lnS * kLog2e;
                         nr.y = y;
+                        nr.zy = zy;
                         nr.pad = 0;
                         info[b] = nr;
                         if (logprob) logprob[t] = lp;
@@ -396,8 +415,8 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
                                 (len % kVec == 0);
             if (ri.mode == 2) {
                 const bool has_y = y >= start && y < start + len;
-                if (vec_ok && nvec == 32 * kVecPerLane && !has_y) {
-                    // full aligned chunk without the label: no per-vector tests
+                if (vec_ok && nvec == 32 * kVecPerLane) {
+                    // full aligned chunk: no per-vector tests
                     Eout* d = dst + lane * kVec;
 #pragma unroll
                     for (int jj = 0; jj < kVecPerLane; ++jj) {
@@ -405,6 +424,15 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
                         unpack_vec<Ein>(q[jj], x);
                         grad_vec_nolabel<kVec>(x, ri, gv);
                         OutVec<Eout>::template store<kVec>(d + 32 * kVec * jj, gv);
+                    }
+                    if (has_y && (int)(((y - start) / kVec) & 31) == lane) {
+                        // The lane that stored the label's vector rewrites the label
+                        // column with w (1 - p_y), p_y from the same arithmetic.
+                        float x8[8], p8[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) x8[e] = ri.zy;
+                        prob8(x8, ri.M, ri.log2S, p8);
+                        dst[y - start] = OutVec<Eout>::one(fmaf(-ri.w, p8[0], ri.w));
                     }
                 } else {
 #pragma unroll
