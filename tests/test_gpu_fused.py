@@ -91,6 +91,33 @@ def test_fused_device_errors(cuda_lib):
     assert torch.all(torch.isnan(g[1])) and torch.all(torch.isnan(g[2]))
 
 
+def test_fused_rows_beyond_the_label_cache(cuda_lib):
+    # Each CTA keeps the labels and weights of its first 384 rows in shared
+    # memory and reads later rows' labels from global memory: give every CTA
+    # more rows than that, with ignored, zero-weight and bad labels among the
+    # late rows, and check the whole batch bit for bit against the two calls.
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    T, V = sms * 390 + 7, 1500
+    g = torch.Generator(device="cuda").manual_seed(11)
+    z = (2.0 * torch.randn(T, V, generator=g, device="cuda")).to(torch.bfloat16)
+    y = torch.randint(0, V, (T,), generator=g, device="cuda")
+    w = torch.randn(T, generator=g, device="cuda")
+    late = torch.arange(sms * 384, T, device="cuda")
+    y[late[::97]] = IGN
+    w[late[5::89]] = 0.0
+    y[late[-3]] = V + 2
+    lp, ent, rs, gg, err = _same_as_two_calls(cuda_lib, z, y, w)
+    assert err & cuda_lib.DEV_BAD_LABEL
+    rows = late[[0, 1, 50, 400, -1]].cpu()
+    zo = to_oracle(z[rows])
+    yo = y[rows].cpu().numpy()
+    ref = oracle.forward(zo, yo, IGN)
+    assert_forward_close(lp[rows.cuda()], ent[rows.cuda()], ref, torch.bfloat16,
+                         what="rows past the label cache")
+    assert_grad_close(gg[rows.cuda()], oracle.backward(zo, yo, w[rows].double().cpu().numpy(), IGN),
+                      torch.bfloat16, "rows past the label cache")
+
+
 def test_fused_tiny_config_against_oracle(cuda_lib):
     from vocab_wide_token_gb300 import inputs
 
@@ -123,3 +150,21 @@ def test_fused_full_size_and_batch_invariance(cuda_lib):
     assert_forward_close(lp[rows], ent[rows], oracle.forward(zo, yo, IGN), torch.bfloat16)
     assert_grad_close(g[rows], oracle.backward(zo, yo, w[rows].double().cpu().numpy(), IGN),
                       torch.bfloat16, "full")
+
+
+@pytest.mark.parametrize("T,block", [(1000, 300), (64, 1024), (1, 1)])
+def test_from_host_equals_device_call(cuda_lib, T, block):
+    # forward_backward_from_host stages row blocks through a double buffer on a
+    # side stream; every output must equal the one-call result bit for bit.
+    V = 4099
+    g = torch.Generator().manual_seed(T)
+    zh = (2.0 * torch.randn(T, V, generator=g)).to(torch.bfloat16).pin_memory()
+    yh = torch.randint(0, V, (T,), generator=g).pin_memory()
+    wh = torch.randn(T, generator=g).pin_memory()
+    if T > 2:
+        yh[1] = IGN
+    ref = cuda_lib.forward_backward(zh.cuda(), yh.cuda(), wh.cuda(), IGN)
+    got = cuda_lib.forward_backward_from_host(zh, yh, wh, IGN, block_rows=block)
+    torch.cuda.synchronize()
+    for a, b, name in zip(ref, got, ("logprob", "entropy", "rowstats", "dlogits")):
+        assert torch.equal(_bits(a), _bits(b)), name

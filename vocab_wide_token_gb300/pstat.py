@@ -267,6 +267,77 @@ def forward_backward(logits: torch.Tensor, labels: torch.Tensor | None,
     return lp, ent, rs, dlogits
 
 
+_side_streams: dict = {}
+
+
+def _side_stream(device: torch.device) -> torch.cuda.Stream:
+    s = _side_streams.get(device)
+    if s is None:
+        s = torch.cuda.Stream(device=device)
+        _side_streams[device] = s
+    return s
+
+
+def forward_backward_from_host(logits: torch.Tensor, labels: torch.Tensor | None,
+                               weights: torch.Tensor | None, ignore_index: int = -100, *,
+                               device=None, out_dtype: torch.dtype | None = None,
+                               block_rows: int = 1024, out=None, dlogits=None, dev_error=None):
+    """forward_backward on logits, labels and weights that live in host memory
+    (pinned, for the copies to run asynchronously).  Row blocks of the logits
+    are copied into a double-buffered device staging area on a side stream
+    while pstat_forward_backward runs on the previous block on the current
+    stream, so after the last copy only one block's kernel remains.  Returns
+    device (logprob, entropy, rowstats, dlogits), complete in stream order on
+    the current stream."""
+    if logits.is_cuda or logits.dim() != 2 or not logits.is_contiguous():
+        raise ValueError("logits must be a contiguous 2-D host tensor")
+    T, V = logits.shape
+    dev = torch.device(device if device is not None else "cuda")
+    if dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+    if block_rows < 1:
+        raise ValueError("block_rows must be positive")
+    cur = torch.cuda.current_stream(dev)
+    side = _side_stream(dev)
+    lab = None if labels is None else labels.to(dev, non_blocking=True)
+    w = None if weights is None else weights.to(dev, non_blocking=True)
+    out_dtype = out_dtype or logits.dtype
+    if out is None:
+        out = (torch.empty(T, dtype=torch.float32, device=dev),
+               torch.empty(T, dtype=torch.float32, device=dev),
+               torch.empty(T, 2, dtype=torch.float32, device=dev))
+    lp, ent, rs = out
+    if dlogits is None:
+        dlogits = torch.empty(T, V, dtype=out_dtype, device=dev)
+    if T == 0:
+        return lp, ent, rs, dlogits
+    B = min(block_rows, T)
+    bufs = [torch.empty(B, V, dtype=logits.dtype, device=dev) for _ in range(2)]
+    for b in bufs:
+        b.record_stream(side)
+    start = torch.cuda.Event()
+    start.record(cur)
+    side.wait_event(start)
+    freed = [None, None]  # event: the kernel that last read this buffer has run
+    for i, r0 in enumerate(range(0, T, B)):
+        r1 = min(T, r0 + B)
+        buf = bufs[i % 2][: r1 - r0]
+        with torch.cuda.stream(side):
+            if freed[i % 2] is not None:
+                side.wait_event(freed[i % 2])
+            buf.copy_(logits[r0:r1], non_blocking=True)
+            copied = torch.cuda.Event()
+            copied.record(side)
+        cur.wait_event(copied)
+        forward_backward(buf, None if lab is None else lab[r0:r1],
+                         None if w is None else w[r0:r1], ignore_index,
+                         out_dtype=out_dtype, out=(lp[r0:r1], ent[r0:r1], rs[r0:r1]),
+                         dlogits=dlogits[r0:r1], dev_error=dev_error)
+        freed[i % 2] = torch.cuda.Event()
+        freed[i % 2].record(cur)
+    return lp, ent, rs, dlogits
+
+
 def log_softmax(logits: torch.Tensor, rowstats: torch.Tensor | None = None, shard_bounds=None,
                 out_dtype: torch.dtype | None = None, *, out=None, workspace=None,
                 dev_error=None):
