@@ -55,7 +55,12 @@ constexpr int BN = 256;            // output columns per tile (MMA N)
 constexpr int BK = 64;             // K per stage: 64 x 16-bit = one 128-byte swizzle row
 constexpr int UK = 16;             // K per tcgen05.mma of kind::f16
 constexpr int STAGES = 4;
-constexpr int STATS_TILES = PSTAT_CHUNK_BF16 / BN;  // 16 tiles per statistics chunk
+// Statistics chunk of the fused forward: 2048 vocabulary columns (8 tiles),
+// folded in ascending tile order by one CTA.  Half the 4096 of the logits
+// path: at V = 151,936 a 16-tile unit leaves some SMs 32 units (512 tiles)
+// against an average of 500; 8-tile units cap that at 504.
+constexpr int LM_CHUNK = 2048;
+constexpr int STATS_TILES = LM_CHUNK / BN;
 constexpr int VC = 8192;           // backward vocabulary chunk (columns staged as G / Gt)
 constexpr int M_GROUP = 32;        // M tiles sharing the L2-resident slice of A
 constexpr int THREADS = 192;
@@ -642,7 +647,7 @@ struct FwdWorkspace {
     size_t stats_off, target_off, total;
 };
 static FwdWorkspace fwd_layout(int64_t T, int64_t V) {
-    const int64_t nc = (V + PSTAT_CHUNK_BF16 - 1) / PSTAT_CHUNK_BF16;
+    const int64_t nc = (V + LM_CHUNK - 1) / LM_CHUNK;
     FwdWorkspace w;
     w.stats_off = 0;
     w.target_off = align_up((size_t)T * nc * kChunkRecordBytes, 256);
@@ -707,7 +712,7 @@ int pstat_lmhead_fused(const void* hidden, const void* W, int64_t T, int64_t V, 
     rc = device_info(&dev);
     if (rc != PSTAT_OK) return rc;
     ShardPlan plan;
-    rc = make_plan(V, PSTAT_CHUNK_BF16, nullptr, 1, &plan);
+    rc = make_plan(V, lm::LM_CHUNK, nullptr, 1, &plan);
     if (rc != PSTAT_OK) return rc;
 
     CUtensorMap map_h, map_w;
