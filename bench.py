@@ -472,7 +472,7 @@ def bench_lmhead(pstat, dev, tflops, tflops_sus, peak_kind, T=16384, steps=3, wa
                                   "unit": "TFLOP/s", "frac": ab / tflops_sus,
                                   "peak_kind": f"{peak_kind} sustained",
                                   "algorithmic_flop": flop_b},
-            "gpu_launches_per_forward": 2, "gpu_launches_per_backward": 1 + 4 * n_chunks}
+            "gpu_launches_per_forward": 2, "gpu_launches_per_backward": 1 + 3 * n_chunks}
 
 
 if __name__ == "__main__":

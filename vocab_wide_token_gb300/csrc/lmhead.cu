@@ -69,16 +69,18 @@ constexpr uint32_t B_BYTES = BN * BK * 2;   // 32 KB
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t TMEM_COLS = 2 * BN;      // double-buffered accumulator
 constexpr uint64_t WAIT_NS = 2000000000ull;
+constexpr int QD = 4;  // depth of the claimed-unit queue (dynamic scheduling)
 
 struct Smem {
     // Offsets inside the 1024-byte aligned dynamic shared memory block.
     static constexpr uint32_t a = 0;
     static constexpr uint32_t b = a + STAGES * A_BYTES;
     static constexpr uint32_t bars = b + STAGES * B_BYTES;
-    // full[STAGES], empty[STAGES], tfull[2], tempty[2], drain
-    static constexpr uint32_t n_bars = 2 * STAGES + 4 + 1;
+    // full[STAGES], empty[STAGES], tfull[2], tempty[2], drain, uq_full[QD], uq_empty[QD]
+    static constexpr uint32_t n_bars = 2 * STAGES + 4 + 1 + 2 * QD;
     static constexpr uint32_t tmem_slot = bars + n_bars * 8;
-    static constexpr uint32_t total = tmem_slot + 16;
+    static constexpr uint32_t uq = tmem_slot + 16;  // int[QD]: claimed unit ids
+    static constexpr uint32_t total = uq + QD * 4;
 };
 constexpr size_t SMEM_BYTES = Smem::total + 1024;  // + alignment slack
 
@@ -104,6 +106,25 @@ __device__ __forceinline__ int unit_tiles(const GemmGeo& g, int un) {
     const int nt = g.n_tiles - un * g.tiles_per_unit;
     return nt < g.tiles_per_unit ? nt : g.tiles_per_unit;
 }
+
+// One launch runs up to two GEMMs with the same epilogue type: units
+// [0, n0) belong to problem 0, [n0, total) to problem 1.  With a claim counter
+// (zeroed before the launch), CTAs take units in index order with atomicAdd,
+// so a CTA that finishes early takes more; without one, unit u goes to CTA
+// u mod gridDim.x.  Either way each tile has exactly one CTA computing it over
+// K in a fixed order, so the results do not depend on the schedule.
+template <class Epi>
+struct Problem {
+    CUtensorMap a, b;
+    GemmGeo g;
+    Epi epi;
+};
+template <class Epi>
+struct Problems {
+    Problem<Epi> p[2];
+    int64_t n0, total;
+    int* counter;  // device int, or nullptr for the static schedule
+};
 
 // Instruction descriptor for fp16 operands (A and B both f16, D fp32).
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
@@ -372,9 +393,7 @@ struct AccumEpi {
 // ---------------------------------------------------------------------------
 template <class Epi, bool kF16>
 __global__ void __launch_bounds__(THREADS, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
-                   const __grid_constant__ CUtensorMap map_b, const GemmGeo g, const Epi epi,
-                   int* __restrict__ dev_error) {
+    tc_gemm_kernel(const __grid_constant__ Problems<Epi> P, int* __restrict__ dev_error) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -384,10 +403,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint64_t* tfull = bars + 2 * STAGES;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
+    uint64_t* uq_full = drain + 1;
+    uint64_t* uq_empty = uq_full + QD;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Smem::tmem_slot);
+    volatile int* uq = reinterpret_cast<volatile int*>(smem + Smem::uq);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const bool dynamic = P.counter != nullptr;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -399,9 +422,17 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&tempty[b], 4);
         }
         mbar_init(drain, 1);
+        for (int q = 0; q < QD; ++q) {
+            mbar_init(&uq_full[q], 1);   // the producer publishes a unit
+            mbar_init(&uq_empty[q], 5);  // the MMA thread and the 4 epilogue warps took it
+        }
         fence_mbar_init();
-        prefetch_tensormap(&map_a);
-        prefetch_tensormap(&map_b);
+        prefetch_tensormap(&P.p[0].a);
+        prefetch_tensormap(&P.p[0].b);
+        if (P.total > P.n0) {
+            prefetch_tensormap(&P.p[1].a);
+            prefetch_tensormap(&P.p[1].b);
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, TMEM_COLS);
@@ -413,19 +444,51 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t tmem_base = *tmem_slot;
     bool failed = false;
 
+    // The i-th unit of this CTA for a consumer role: round robin, or popped
+    // from the queue the producer fills.  -1 ends the loop; -2 is a timeout.
+    auto consume_unit = [&](int64_t i, bool arrive) -> int64_t {
+        if (!dynamic) {
+            const int64_t u = (int64_t)blockIdx.x + i * gridDim.x;
+            return u < P.total ? u : -1;
+        }
+        const int q = (int)(i % QD);
+        if (!mbar_wait_bounded(&uq_full[q], (uint32_t)((i / QD) & 1), WAIT_NS)) return -2;
+        const int64_t u = uq[q];
+        if (arrive) mbar_arrive(&uq_empty[q]);
+        return u;
+    };
+
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
             const uint64_t pol_a = policy_evict_last();
             const uint64_t pol_b = policy_evict_first();
             uint32_t it = 0;
-            for (int64_t u = blockIdx.x; u < g.n_units && !failed; u += gridDim.x) {
+            for (int64_t i = 0; !failed; ++i) {
+                int64_t u;
+                if (dynamic) {
+                    const int q = (int)(i % QD);
+                    if (!mbar_wait_bounded(&uq_empty[q], (uint32_t)(((i / QD) & 1) ^ 1), WAIT_NS)) {
+                        failed = true;
+                        break;
+                    }
+                    u = atomicAdd(P.counter, 1);
+                    if (u >= P.total) u = -1;
+                    uq[q] = (int)u;
+                    mbar_arrive(&uq_full[q]);
+                } else {
+                    u = (int64_t)blockIdx.x + i * gridDim.x;
+                    if (u >= P.total) u = -1;
+                }
+                if (u < 0) break;
+                const int w = u < P.n0 ? 0 : 1;
+                const Problem<Epi>& pr = P.p[w];
                 int m, un;
-                unit_coords(g, u, m, un);
-                const int nt = unit_tiles(g, un);
+                unit_coords(pr.g, u - (w ? P.n0 : 0), m, un);
+                const int nt = unit_tiles(pr.g, un);
                 for (int j = 0; j < nt && !failed; ++j) {
-                    const int n = un * g.tiles_per_unit + j;
-                    for (int kb = 0; kb < g.k_blocks; ++kb, ++it) {
+                    const int n = un * pr.g.tiles_per_unit + j;
+                    for (int kb = 0; kb < pr.g.k_blocks; ++kb, ++it) {
                         const int s = it % STAGES;
                         const uint32_t ph = (it / STAGES) & 1u;
                         if (!mbar_wait_bounded(&empty[s], ph ^ 1u, WAIT_NS)) {
@@ -433,10 +496,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                             break;
                         }
                         mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-                        tma_load_2d(smem + Smem::a + s * A_BYTES, &map_a, kb * BK, m * BM,
+                        tma_load_2d(smem + Smem::a + s * A_BYTES, &pr.a, kb * BK, m * BM,
                                     &full[s], pol_a);
-                        tma_load_2d(smem + Smem::b + s * B_BYTES, &map_b, kb * BK,
-                                    g.b_row0 + n * BN, &full[s], pol_b);
+                        tma_load_2d(smem + Smem::b + s * B_BYTES, &pr.b, kb * BK,
+                                    pr.g.b_row0 + n * BN, &full[s], pol_b);
                     }
                 }
             }
@@ -453,9 +516,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) {
             constexpr uint32_t idesc = kF16 ? idesc_f16_f32(BM, BN) : idesc_bf16_f32(BM, BN);
             uint32_t it = 0, tc = 0;
-            for (int64_t u = blockIdx.x; u < g.n_units && !failed; u += gridDim.x) {
+            for (int64_t i = 0; !failed; ++i) {
+                const int64_t u = consume_unit(i, true);
+                if (u == -2) failed = true;
+                if (u < 0) break;
+                const int w = u < P.n0 ? 0 : 1;
+                const GemmGeo& g = P.p[w].g;
                 int m, un;
-                unit_coords(g, u, m, un);
+                unit_coords(g, u - (w ? P.n0 : 0), m, un);
                 const int nt = unit_tiles(g, un);
                 for (int j = 0; j < nt && !failed; ++j, ++tc) {
                     const uint32_t b = tc & 1u;
@@ -498,13 +566,21 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int row = q * 32 + lane;
         uint32_t tc = 0;
         typename Epi::State st;
-        for (int64_t u = blockIdx.x; u < g.n_units && !failed; u += gridDim.x) {
+        for (int64_t i = 0; !failed; ++i) {
+            int64_t u = consume_unit(i, false);
+            __syncwarp();
+            if (dynamic && lane == 0 && u != -2) mbar_arrive(&uq_empty[i % QD]);
+            u = __shfl_sync(0xFFFFFFFFu, u, 0);
+            if (u == -2) failed = true;
+            if (u < 0) break;
+            const int w = u < P.n0 ? 0 : 1;
+            const Problem<Epi>& pr = P.p[w];
             int m, un;
-            unit_coords(g, u, m, un);
-            const int nt = unit_tiles(g, un);
-            epi.unit_begin(st, m, un, row);
+            unit_coords(pr.g, u - (w ? P.n0 : 0), m, un);
+            const int nt = unit_tiles(pr.g, un);
+            pr.epi.unit_begin(st, m, un, row);
             for (int j = 0; j < nt; ++j, ++tc) {
-                const int n = un * g.tiles_per_unit + j;
+                const int n = un * pr.g.tiles_per_unit + j;
                 const uint32_t b = tc & 1u;
                 const uint32_t tph = (tc >> 1) & 1u;
                 bool ok = mbar_wait_bounded(&tfull[b], tph, WAIT_NS);
@@ -514,14 +590,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                epi.tile(st, tmem_base + ((uint32_t)(q * 32) << 16) + b * BN, m, n, row);
+                pr.epi.tile(st, tmem_base + ((uint32_t)(q * 32) << 16) + b * BN, m, n, row);
                 // accumulator b may be overwritten from here on
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tempty[b]);
             }
             if (failed) break;
-            epi.unit_end(st, m, un, row);
+            pr.epi.unit_end(st, m, un, row);
         }
     }
 
@@ -614,8 +690,8 @@ static GemmGeo geo(int64_t M, int64_t N, int64_t K, int tiles_per_unit, int64_t 
 }
 
 template <class Epi, bool kF16>
-static cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmGeo& g,
-                               const Epi& epi, int* dev_error, int sm_count, cudaStream_t st) {
+static cudaError_t launch_problems(const Problems<Epi>& P, int* dev_error, int sm_count,
+                                   cudaStream_t st) {
     static std::atomic<bool> configured[64];
     int devi = 0;
     cudaGetDevice(&devi);
@@ -626,11 +702,48 @@ static cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, con
         if (e != cudaSuccess) return e;
         if (devi < 64) configured[devi].store(true);
     }
-    if (g.n_units == 0) return cudaSuccess;
-    const int64_t grid = g.n_units < sm_count ? g.n_units : sm_count;
-    tc_gemm_kernel<Epi, kF16><<<(unsigned)grid, THREADS, SMEM_BYTES, st>>>(ma, mb, g, epi,
-                                                                          dev_error);
+    if (P.total == 0) return cudaSuccess;
+    const int64_t grid = P.total < sm_count ? P.total : sm_count;
+    tc_gemm_kernel<Epi, kF16><<<(unsigned)grid, THREADS, SMEM_BYTES, st>>>(P, dev_error);
     return cudaGetLastError();
+}
+
+// One GEMM, static round-robin schedule.
+template <class Epi, bool kF16>
+static cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmGeo& g,
+                               const Epi& epi, int* dev_error, int sm_count, cudaStream_t st) {
+    Problems<Epi> P;
+    P.p[0].a = ma;
+    P.p[0].b = mb;
+    P.p[0].g = g;
+    P.p[0].epi = epi;
+    P.p[1] = P.p[0];
+    P.n0 = g.n_units;
+    P.total = g.n_units;
+    P.counter = nullptr;
+    return launch_problems<Epi, kF16>(P, dev_error, sm_count, st);
+}
+
+// Two GEMMs in one launch, units claimed through `counter` (zeroed before).
+// The first problem should be the one with the longer units.
+template <class Epi, bool kF16>
+static cudaError_t launch_gemm_pair(const CUtensorMap& ma0, const CUtensorMap& mb0,
+                                    const GemmGeo& g0, const Epi& e0, const CUtensorMap& ma1,
+                                    const CUtensorMap& mb1, const GemmGeo& g1, const Epi& e1,
+                                    int* counter, int* dev_error, int sm_count, cudaStream_t st) {
+    Problems<Epi> P;
+    P.p[0].a = ma0;
+    P.p[0].b = mb0;
+    P.p[0].g = g0;
+    P.p[0].epi = e0;
+    P.p[1].a = ma1;
+    P.p[1].b = mb1;
+    P.p[1].g = g1;
+    P.p[1].epi = e1;
+    P.n0 = g0.n_units;
+    P.total = g0.n_units + g1.n_units;
+    P.counter = counter;
+    return launch_problems<Epi, kF16>(P, dev_error, sm_count, st);
 }
 
 static cudaError_t launch_transpose(const uint16_t* src, int64_t rows, int64_t cols,
@@ -657,16 +770,19 @@ static FwdWorkspace fwd_layout(int64_t T, int64_t V) {
 
 struct BwdWorkspace {
     int64_t Tp;  // T padded to whole M tiles
-    size_t hT_off, Wt_off, G_off, Gt_off, total;
+    size_t hT_off, Wt_off, G_off, Gt_off, ctr_off, total;
+    int64_t n_chunks;  // vocabulary chunks of VC columns
 };
-static BwdWorkspace bwd_layout(int64_t T, int64_t d) {
+static BwdWorkspace bwd_layout(int64_t T, int64_t V, int64_t d) {
     BwdWorkspace w;
     w.Tp = (T + BM - 1) / BM * BM;
     w.hT_off = 0;                                                 // [d, Tp] fp16
     w.Wt_off = align_up(w.hT_off + (size_t)d * w.Tp * 2, 1024);  // [d, VC] fp16
     w.G_off = align_up(w.Wt_off + (size_t)d * VC * 2, 1024);     // [Tp, VC] fp16
     w.Gt_off = align_up(w.G_off + (size_t)w.Tp * VC * 2, 1024);  // [VC, Tp] fp16
-    w.total = align_up(w.Gt_off + (size_t)VC * w.Tp * 2, 1024);
+    w.ctr_off = align_up(w.Gt_off + (size_t)VC * w.Tp * 2, 1024);  // int[n_chunks]
+    w.n_chunks = (V + VC - 1) / VC;
+    w.total = align_up(w.ctr_off + (size_t)w.n_chunks * sizeof(int), 1024);
     return w;
 }
 
@@ -691,7 +807,7 @@ int pstat_lmhead_workspace_size(int64_t T, int64_t V, int64_t d, size_t* bytes) 
     if (!bytes) return PSTAT_ERR_NULLPTR;
     if (T < 0 || V < 1 || d < lm::BK || d % lm::BK != 0) return PSTAT_ERR_SHAPE;
     const size_t f = lm::fwd_layout(T, V).total;
-    const size_t b = lm::bwd_layout(T, d).total;
+    const size_t b = lm::bwd_layout(T, V, d).total;
     *bytes = f > b ? f : b;
     return PSTAT_OK;
 }
@@ -752,7 +868,7 @@ int pstat_lmhead_backward(const void* hidden, const void* W, int64_t T, int64_t 
         (labels && (reinterpret_cast<uintptr_t>(labels) & 7u)) ||
         (weights && (reinterpret_cast<uintptr_t>(weights) & 3u)))
         return PSTAT_ERR_ALIGN;
-    const lm::BwdWorkspace wl = lm::bwd_layout(T, d);
+    const lm::BwdWorkspace wl = lm::bwd_layout(T, V, d);
     if (!workspace || ws_bytes < wl.total) return PSTAT_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) & 1023u) return PSTAT_ERR_ALIGN;
     DeviceInfo dev;
@@ -794,7 +910,10 @@ int pstat_lmhead_backward(const void* hidden, const void* W, int64_t T, int64_t 
     ge.ldgt = Tp;
     ge.dev_error = dev_error;
 
-    const int64_t n_chunks = (V + lm::VC - 1) / lm::VC;
+    const int64_t n_chunks = wl.n_chunks;
+    int* ctr = reinterpret_cast<int*>(ws + wl.ctr_off);  // one unit counter per chunk
+    if (cudaMemsetAsync(ctr, 0, (size_t)n_chunks * sizeof(int), st) != cudaSuccess)
+        return PSTAT_ERR_CUDA;
     for (int64_t c = 0; c < n_chunks; ++c) {
         const int64_t c0 = c * lm::VC;
         const int64_t vc = (V - c0) < lm::VC ? (V - c0) : lm::VC;
@@ -808,7 +927,9 @@ int pstat_lmhead_backward(const void* hidden, const void* W, int64_t T, int64_t 
         if (lm::launch_gemm<lm::GradEpi, false>(map_h, map_w, g1, ge, dev_error, dev.sm_count,
                                                 st) != cudaSuccess)
             return PSTAT_ERR_CUDA;
-        // 2. dhidden += G W_c
+        // 2. dhidden += G W_c  and  3. dW[c0 : c0 + vc] += Gt hidden, in one
+        // launch: CTAs claim units of both GEMMs (the longer-K one first)
+        // from this chunk's counter, so neither leaves a partial last wave.
         lm::AccumEpi e2;
         e2.out = dhidden;
         e2.ld = d;
@@ -816,10 +937,6 @@ int pstat_lmhead_backward(const void* hidden, const void* W, int64_t T, int64_t 
         e2.rows = T;
         e2.cols = d;
         const lm::GemmGeo g2 = lm::geo(T, d, vc, 1, 0);
-        if (lm::launch_gemm<lm::AccumEpi, true>(map_G, map_Wt, g2, e2, dev_error, dev.sm_count,
-                                                st) != cudaSuccess)
-            return PSTAT_ERR_CUDA;
-        // 3. dW[c0 : c0 + vc] += Gt hidden
         lm::AccumEpi e3;
         e3.out = dW;
         e3.ld = d;
@@ -827,9 +944,15 @@ int pstat_lmhead_backward(const void* hidden, const void* W, int64_t T, int64_t 
         e3.rows = vc;
         e3.cols = d;
         const lm::GemmGeo g3 = lm::geo(vc, d, Tp, 1, 0);
-        if (lm::launch_gemm<lm::AccumEpi, true>(map_Gt, map_hT, g3, e3, dev_error, dev.sm_count,
-                                                st) != cudaSuccess)
-            return PSTAT_ERR_CUDA;
+        const cudaError_t e =
+            g3.k_blocks >= g2.k_blocks
+                ? lm::launch_gemm_pair<lm::AccumEpi, true>(map_Gt, map_hT, g3, e3, map_G, map_Wt,
+                                                           g2, e2, ctr + c, dev_error,
+                                                           dev.sm_count, st)
+                : lm::launch_gemm_pair<lm::AccumEpi, true>(map_G, map_Wt, g2, e2, map_Gt, map_hT,
+                                                           g3, e3, ctr + c, dev_error,
+                                                           dev.sm_count, st);
+        if (e != cudaSuccess) return PSTAT_ERR_CUDA;
     }
     return PSTAT_OK;
 }
