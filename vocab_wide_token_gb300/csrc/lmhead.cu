@@ -755,6 +755,26 @@ static cudaError_t launch_transpose(const uint16_t* src, int64_t rows, int64_t c
     return cudaGetLastError();
 }
 
+// A stream and events of one backward call: the W transposes run there, next
+// to the GEMMs on the caller's stream.  Created per call and released at the
+// end of it (destruction waits for nothing; the driver frees them once their
+// work is done), so concurrent calls never share them.
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t start = nullptr, hT = nullptr, done = nullptr, tr[2] = {}, acc[2] = {};
+    bool ok = false;
+    SideStream() {
+        ok = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) == cudaSuccess;
+        for (cudaEvent_t* e : {&start, &hT, &done, &tr[0], &tr[1], &acc[0], &acc[1]})
+            ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
+    }
+    ~SideStream() {
+        for (cudaEvent_t e : {start, hT, done, tr[0], tr[1], acc[0], acc[1]})
+            if (e) cudaEventDestroy(e);
+        if (s) cudaStreamDestroy(s);
+    }
+};
+
 // ---- workspace layouts -------------------------------------------------------------
 struct FwdWorkspace {
     size_t stats_off, target_off, total;
@@ -770,15 +790,16 @@ static FwdWorkspace fwd_layout(int64_t T, int64_t V) {
 
 struct BwdWorkspace {
     int64_t Tp;  // T padded to whole M tiles
-    size_t hT_off, Wt_off, G_off, Gt_off, ctr_off, total;
+    size_t hT_off, Wt_off[2], G_off, Gt_off, ctr_off, total;
     int64_t n_chunks;  // vocabulary chunks of VC columns
 };
 static BwdWorkspace bwd_layout(int64_t T, int64_t V, int64_t d) {
     BwdWorkspace w;
     w.Tp = (T + BM - 1) / BM * BM;
     w.hT_off = 0;                                                 // [d, Tp] fp16
-    w.Wt_off = align_up(w.hT_off + (size_t)d * w.Tp * 2, 1024);  // [d, VC] fp16
-    w.G_off = align_up(w.Wt_off + (size_t)d * VC * 2, 1024);     // [Tp, VC] fp16
+    w.Wt_off[0] = align_up(w.hT_off + (size_t)d * w.Tp * 2, 1024);  // [d, VC] fp16, two
+    w.Wt_off[1] = align_up(w.Wt_off[0] + (size_t)d * VC * 2, 1024); // (chunks alternate)
+    w.G_off = align_up(w.Wt_off[1] + (size_t)d * VC * 2, 1024);     // [Tp, VC] fp16
     w.Gt_off = align_up(w.G_off + (size_t)w.Tp * VC * 2, 1024);  // [VC, Tp] fp16
     w.ctr_off = align_up(w.Gt_off + (size_t)VC * w.Tp * 2, 1024);  // int[n_chunks]
     w.n_chunks = (V + VC - 1) / VC;
@@ -877,24 +898,21 @@ int pstat_lmhead_backward(const void* hidden, const void* W, int64_t T, int64_t 
 
     char* ws = static_cast<char*>(workspace);
     __half* hT = reinterpret_cast<__half*>(ws + wl.hT_off);
-    __half* Wt = reinterpret_cast<__half*>(ws + wl.Wt_off);
+    __half* Wt[2] = {reinterpret_cast<__half*>(ws + wl.Wt_off[0]),
+                     reinterpret_cast<__half*>(ws + wl.Wt_off[1])};
     __half* G = reinterpret_cast<__half*>(ws + wl.G_off);
     __half* Gt = reinterpret_cast<__half*>(ws + wl.Gt_off);
     const int64_t Tp = wl.Tp;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
-    CUtensorMap map_h, map_w, map_G, map_Wt, map_Gt, map_hT;
+    CUtensorMap map_h, map_w, map_G, map_Wt[2], map_Gt, map_hT;
     if (!lm::make_map(&map_h, false, hidden, T, d, d, lm::BM) ||
         !lm::make_map(&map_w, false, W, V, d, d, lm::BN) ||
         !lm::make_map(&map_G, true, G, Tp, lm::VC, lm::VC, lm::BM) ||
-        !lm::make_map(&map_Wt, true, Wt, d, lm::VC, lm::VC, lm::BN) ||
+        !lm::make_map(&map_Wt[0], true, Wt[0], d, lm::VC, lm::VC, lm::BN) ||
+        !lm::make_map(&map_Wt[1], true, Wt[1], d, lm::VC, lm::VC, lm::BN) ||
         !lm::make_map(&map_Gt, true, Gt, lm::VC, Tp, Tp, lm::BM) ||
         !lm::make_map(&map_hT, true, hT, d, Tp, Tp, lm::BN))
-        return PSTAT_ERR_CUDA;
-
-    // hidden^T once (fp16, tokens padded to Tp with zeros)
-    if (lm::launch_transpose(static_cast<const uint16_t*>(hidden), T, d, d, hT, Tp, Tp, dev_error,
-                             st) != cudaSuccess)
         return PSTAT_ERR_CUDA;
 
     lm::GradEpi ge;
@@ -914,18 +932,48 @@ int pstat_lmhead_backward(const void* hidden, const void* W, int64_t T, int64_t 
     int* ctr = reinterpret_cast<int*>(ws + wl.ctr_off);  // one unit counter per chunk
     if (cudaMemsetAsync(ctr, 0, (size_t)n_chunks * sizeof(int), st) != cudaSuccess)
         return PSTAT_ERR_CUDA;
-    for (int64_t c = 0; c < n_chunks; ++c) {
+
+    // The transposes (hidden once, W_c per chunk into alternating buffers) run
+    // on a side stream: W_{c+1} is transposed while chunk c's GEMMs run, after
+    // the GEMMs of chunk c-1 (the last reader of its buffer) are done.
+    lm::SideStream x;
+    if (!x.ok) return PSTAT_ERR_CUDA;
+    auto transpose_w = [&](int64_t c) {
         const int64_t c0 = c * lm::VC;
         const int64_t vc = (V - c0) < lm::VC ? (V - c0) : lm::VC;
         // W_c^T (fp16; vocabulary columns past the chunk end as zeros)
-        if (lm::launch_transpose(static_cast<const uint16_t*>(W) + c0 * d, vc, d, d, Wt, lm::VC,
-                                 lm::VC, dev_error, st) != cudaSuccess)
-            return PSTAT_ERR_CUDA;
+        return lm::launch_transpose(static_cast<const uint16_t*>(W) + c0 * d, vc, d, d,
+                                    Wt[c & 1], lm::VC, lm::VC, dev_error, x.s);
+    };
+    if (cudaEventRecord(x.start, st) != cudaSuccess ||
+        cudaStreamWaitEvent(x.s, x.start, 0) != cudaSuccess)
+        return PSTAT_ERR_CUDA;
+    // hidden^T once (fp16, tokens padded to Tp with zeros)
+    if (lm::launch_transpose(static_cast<const uint16_t*>(hidden), T, d, d, hT, Tp, Tp, dev_error,
+                             x.s) != cudaSuccess ||
+        cudaEventRecord(x.hT, x.s) != cudaSuccess || transpose_w(0) != cudaSuccess ||
+        cudaEventRecord(x.tr[0], x.s) != cudaSuccess)
+        return PSTAT_ERR_CUDA;
+
+    for (int64_t c = 0; c < n_chunks; ++c) {
+        const int64_t c0 = c * lm::VC;
+        const int64_t vc = (V - c0) < lm::VC ? (V - c0) : lm::VC;
+        const int b = (int)(c & 1);
+        if (c + 1 < n_chunks) {
+            if (c >= 1 && cudaStreamWaitEvent(x.s, x.acc[b ^ 1], 0) != cudaSuccess)
+                return PSTAT_ERR_CUDA;
+            if (transpose_w(c + 1) != cudaSuccess ||
+                cudaEventRecord(x.tr[b ^ 1], x.s) != cudaSuccess)
+                return PSTAT_ERR_CUDA;
+        }
         // 1. recompute the chunk's logits -> G, Gt
         ge.c0 = c0;
         const lm::GemmGeo g1 = lm::geo(Tp, vc, d, 1, c0);
         if (lm::launch_gemm<lm::GradEpi, false>(map_h, map_w, g1, ge, dev_error, dev.sm_count,
                                                 st) != cudaSuccess)
+            return PSTAT_ERR_CUDA;
+        if (cudaStreamWaitEvent(st, x.tr[b], 0) != cudaSuccess ||
+            (c == 0 && cudaStreamWaitEvent(st, x.hT, 0) != cudaSuccess))
             return PSTAT_ERR_CUDA;
         // 2. dhidden += G W_c  and  3. dW[c0 : c0 + vc] += Gt hidden, in one
         // launch: CTAs claim units of both GEMMs (the longer-K one first)
@@ -946,14 +994,19 @@ int pstat_lmhead_backward(const void* hidden, const void* W, int64_t T, int64_t 
         const lm::GemmGeo g3 = lm::geo(vc, d, Tp, 1, 0);
         const cudaError_t e =
             g3.k_blocks >= g2.k_blocks
-                ? lm::launch_gemm_pair<lm::AccumEpi, true>(map_Gt, map_hT, g3, e3, map_G, map_Wt,
-                                                           g2, e2, ctr + c, dev_error,
+                ? lm::launch_gemm_pair<lm::AccumEpi, true>(map_Gt, map_hT, g3, e3, map_G,
+                                                           map_Wt[b], g2, e2, ctr + c, dev_error,
                                                            dev.sm_count, st)
-                : lm::launch_gemm_pair<lm::AccumEpi, true>(map_G, map_Wt, g2, e2, map_Gt, map_hT,
-                                                           g3, e3, ctr + c, dev_error,
+                : lm::launch_gemm_pair<lm::AccumEpi, true>(map_G, map_Wt[b], g2, e2, map_Gt,
+                                                           map_hT, g3, e3, ctr + c, dev_error,
                                                            dev.sm_count, st);
-        if (e != cudaSuccess) return PSTAT_ERR_CUDA;
+        if (e != cudaSuccess || cudaEventRecord(x.acc[b], st) != cudaSuccess)
+            return PSTAT_ERR_CUDA;
     }
+    // join: the side stream's work precedes whatever the caller queues next
+    if (cudaEventRecord(x.done, x.s) != cudaSuccess ||
+        cudaStreamWaitEvent(st, x.done, 0) != cudaSuccess)
+        return PSTAT_ERR_CUDA;
     return PSTAT_OK;
 }
 
