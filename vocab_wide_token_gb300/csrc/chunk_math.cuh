@@ -336,19 +336,53 @@ __device__ __forceinline__ uint16_t out_cast(float g, uint16_t*) {
 }
 __device__ __forceinline__ float out_cast(float g, float*) { return g; }
 
-// p = e^(z - M - ln S) for 8 elements.
-__device__ __forceinline__ void prob8(const float (&x)[8], float M, float log2S, float (&p)[8]) {
-    const uint64_t negM = f2_pack(-M, -M);
+// Element-wise softmax for the gradient.  With m2 = RN(M log2e) and its exact
+// residual delta = M log2e - m2 (one FMA),
+//     e^(z - M - ln S) = 2^(RN(z log2e - m2)) * K,   K = 2^-(RN(ln S log2e + delta)),
+// up to roundings, so an element costs one packed FMA and one exp2 -- the
+// form of the chunk statistics -- and the row factor K (times -w) rides on
+// the multiply the gradient needs anyway.  The row constants depend on
+// (M, ln S, w) only, so every kernel that forms the gradient from the same
+// row statistics produces the same bits.
+struct GradRow {
+    float m2;   // RN(M log2e)
+    float K;    // 2^-(ln S log2e + delta)
+    float nwK;  // -w K
+    float w;
+};
+__device__ __forceinline__ GradRow grad_row(float M, float lnS, float w) {
+    GradRow r;
+    r.m2 = M * kLog2e;
+    const float delta = fmaf(M, kLog2e, -r.m2);
+    r.K = exp2f(-fmaf(lnS, kLog2e, delta));
+    r.nwK = -w * r.K;
+    r.w = w;
+    return r;
+}
+
+// e_i = 2^(RN(x_i log2e - m2)) for 8 elements.
+__device__ __forceinline__ void exp8(const float (&x)[8], float m2, float (&e)[8]) {
     const uint64_t l2e = f2_pack(kLog2e, kLog2e);
-    const uint64_t nl2s = f2_pack(-log2S, -log2S);
+    const uint64_t nm2 = f2_pack(-m2, -m2);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const uint64_t d = f2_add(f2_pack(x[2 * i], x[2 * i + 1]), negM);
         float a0, a1;
-        f2_unpack(f2_fma(d, l2e, nl2s), a0, a1);
-        p[2 * i] = ex2_approx(a0);
-        p[2 * i + 1] = ex2_approx(a1);
+        f2_unpack(f2_fma(f2_pack(x[2 * i], x[2 * i + 1]), l2e, nm2), a0, a1);
+        e[2 * i] = ex2_approx(a0);
+        e[2 * i + 1] = ex2_approx(a1);
     }
+}
+
+// g_i = -w p_i = e_i (-w K) for 8 elements (the label column is fixed by the caller).
+__device__ __forceinline__ void grad8(const float (&e)[8], const GradRow& r, float (&g)[8]) {
+    const uint64_t k = f2_pack(r.nwK, r.nwK);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f2_unpack(f2_mul(f2_pack(e[2 * i], e[2 * i + 1]), k), g[2 * i], g[2 * i + 1]);
+}
+
+// The label column: w (1 - p_y) with p_y = e_y K.
+__device__ __forceinline__ float grad_label(float e_y, const GradRow& r) {
+    return fmaf(-r.w, e_y * r.K, r.w);
 }
 
 }  // namespace pstat

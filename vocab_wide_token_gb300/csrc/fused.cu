@@ -39,11 +39,10 @@ constexpr int kFbWarps = 13;
 constexpr int kFbStages = 2;  // bulk-copy slots per warp
 
 struct RowInfo {
-    float M, log2S, w;
-    int mode;  // 0: all-zero row, 1: NaN row, 2: compute
+    GradRow gr;  // gradient constants from (M, ln S, w) (mode 2)
+    int mode;    // 0: all-zero row, 1: NaN row, 2: compute
+    float zy;    // the label's logit (mode 2)
     long long y;
-    float zy;  // the label's logit (mode 2)
-    int pad;
 };
 
 constexpr size_t kRingBytes = (size_t)kFbWarps * kFbStages * kSlotBytes;
@@ -94,29 +93,33 @@ struct OutVec<float> {
     __device__ static float one(float g) { return g; }
 };
 
-// The backward kernel's element arithmetic for N = 4 or 8 elements.
+// The backward kernel's element arithmetic for N = 4 or 8 elements (N = 4:
+// the fp32 vector is evaluated as the first half of an 8-element one).
+template <int N>
+__device__ __forceinline__ void exp_vec(const float (&x)[N], const GradRow& r, float (&e)[N]) {
+    if constexpr (N == 8) {
+        exp8(x, r.m2, e);
+    } else {
+        float x8[8] = {x[0], x[1], x[2], x[3], x[0], x[1], x[2], x[3]};
+        float e8[8];
+        exp8(x8, r.m2, e8);
+#pragma unroll
+        for (int i = 0; i < N; ++i) e[i] = e8[i];
+    }
+}
 template <int N>
 __device__ __forceinline__ void grad_vec(const float (&x)[N], const RowInfo& ri, int64_t col0,
                                          int64_t y, float (&g)[N]) {
-    float p[N];
-    if constexpr (N == 8) {
-        prob8(x, ri.M, ri.log2S, p);
-    } else {
-        float x8[8] = {x[0], x[1], x[2], x[3], x[0], x[1], x[2], x[3]};
-        float p8[8];
-        prob8(x8, ri.M, ri.log2S, p8);
+    float e[N];
+    exp_vec<N>(x, ri.gr, e);
+    const uint64_t k = f2_pack(ri.gr.nwK, ri.gr.nwK);
 #pragma unroll
-        for (int i = 0; i < N; ++i) p[i] = p8[i];
-    }
-    const float negw = -ri.w;
-    const uint64_t nw = f2_pack(negw, negw);
-#pragma unroll
-    for (int i = 0; i < N; i += 2) f2_unpack(f2_mul(f2_pack(p[i], p[i + 1]), nw), g[i], g[i + 1]);
+    for (int i = 0; i < N; i += 2) f2_unpack(f2_mul(f2_pack(e[i], e[i + 1]), k), g[i], g[i + 1]);
     const int64_t r = y - col0;
     if (r >= 0 && r < N) {
 #pragma unroll
-        for (int e = 0; e < N; ++e)
-            if (e == r) g[e] = fmaf(negw, p[e], ri.w);  // w (1 - p_y)
+        for (int i = 0; i < N; ++i)
+            if (i == r) g[i] = grad_label(e[i], ri.gr);  // w (1 - p_y)
     }
 }
 
@@ -124,20 +127,11 @@ __device__ __forceinline__ void grad_vec(const float (&x)[N], const RowInfo& ri,
 template <int N>
 __device__ __forceinline__ void grad_vec_nolabel(const float (&x)[N], const RowInfo& ri,
                                                  float (&g)[N]) {
-    float p[N];
-    if constexpr (N == 8) {
-        prob8(x, ri.M, ri.log2S, p);
-    } else {
-        float x8[8] = {x[0], x[1], x[2], x[3], x[0], x[1], x[2], x[3]};
-        float p8[8];
-        prob8(x8, ri.M, ri.log2S, p8);
+    float e[N];
+    exp_vec<N>(x, ri.gr, e);
+    const uint64_t k = f2_pack(ri.gr.nwK, ri.gr.nwK);
 #pragma unroll
-        for (int i = 0; i < N; ++i) p[i] = p8[i];
-    }
-    const float negw = -ri.w;
-    const uint64_t nw = f2_pack(negw, negw);
-#pragma unroll
-    for (int i = 0; i < N; i += 2) f2_unpack(f2_mul(f2_pack(p[i], p[i + 1]), nw), g[i], g[i + 1]);
+    for (int i = 0; i < N; i += 2) f2_unpack(f2_mul(f2_pack(e[i], e[i + 1]), k), g[i], g[i + 1]);
 }
 
 template <typename Ein>
@@ -291,7 +285,7 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
     int64_t pc = 0;
     uint32_t phase = 0;  // parity bit per ring slot
     bool failed = false;
-    RowInfo ri = {0.f, 0.f, 0.f, 0, 0, 0.f, 0};
+    RowInfo ri = {{0.f, 0.f, 0.f, 0.f}, 0, 0.f, 0};
     while (!done(cc)) {
         const Task tk = task_of(cc);
         const int b = (int)(tk.r & 1);
@@ -367,7 +361,6 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
                         int err = 0;
                         float lnS, H, lp;
                         RowInfo nr;
-                        nr.w = w;
                         if (!(M > -INFINITY)) {
                             err |= PSTAT_DEV_EMPTY_ROW;
                             lnS = NAN;
@@ -392,11 +385,9 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
                             nr.mode = 1;
                         else
                             nr.mode = 2;
-                        nr.M = M;
-                        nr.log2S = lnS * kLog2e;
+                        nr.gr = nr.mode == 2 ? grad_row(M, lnS, w) : GradRow{0.f, 0.f, 0.f, 0.f};
                         nr.y = y;
                         nr.zy = zy;
-                        nr.pad = 0;
                         info[b] = nr;
                         if (logprob) logprob[t] = lp;
                         if (entropy) entropy[t] = H;
@@ -427,12 +418,12 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
                     }
                     if (has_y && (int)(((y - start) / kVec) & 31) == lane) {
                         // The lane that stored the label's vector rewrites the label
-                        // column with w (1 - p_y), p_y from the same arithmetic.
-                        float x8[8], p8[8];
+                        // column with w (1 - p_y), e_y from the same arithmetic.
+                        float x8[8], e8[8];
 #pragma unroll
                         for (int e = 0; e < 8; ++e) x8[e] = ri.zy;
-                        prob8(x8, ri.M, ri.log2S, p8);
-                        dst[y - start] = OutVec<Eout>::one(fmaf(-ri.w, p8[0], ri.w));
+                        exp8(x8, ri.gr.m2, e8);
+                        dst[y - start] = OutVec<Eout>::one(grad_label(e8[0], ri.gr));
                     }
                 } else {
 #pragma unroll

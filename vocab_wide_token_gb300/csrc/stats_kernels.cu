@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(kBwdThreads)
     const int64_t y = labels ? labels[t] : ignore_index;
     const float w = weights ? weights[t] : 1.f;
     int mode;  // 0: zero row, 1: NaN row, 2: compute
-    float M = 0.f, log2S = 0.f;
+    GradRow row = {0.f, 0.f, 0.f, 0.f};
     if (y == ignore_index || w == 0.f) {
         mode = 0;
     } else {
@@ -248,15 +248,13 @@ __global__ void __launch_bounds__(kBwdThreads)
                 atomicOr(dev_error, (y < 0 || y >= V) ? PSTAT_DEV_BAD_LABEL : PSTAT_DEV_EMPTY_ROW);
         } else {
             mode = 2;
-            M = rs.x;
-            log2S = rs.y * kLog2e;
+            row = grad_row(rs.x, rs.y, w);
         }
     }
     const float fill = (mode == 0) ? 0.f : NAN;
     const bool vec_ok = ((reinterpret_cast<uintptr_t>(zin + c0) & 15u) == 0) &&
                         ((reinterpret_cast<uintptr_t>(zout + c0) & 15u) == 0);
     const int64_t nv = vec_ok ? (c1 - c0) >> 3 : 0;
-    const float negw = -w;
 
     for (int64_t base = 0; base < nv; base += (int64_t)kBwdThreads * kBwdUnroll) {
         float x[kBwdUnroll][8];
@@ -272,17 +270,14 @@ __global__ void __launch_bounds__(kBwdThreads)
             if (col[k] < 0) continue;
             float g[8];
             if (mode == 2) {
-                float p[8];
-                prob8(x[k], M, log2S, p);
-                const uint64_t nw = f2_pack(negw, negw);
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    f2_unpack(f2_mul(f2_pack(p[2 * i], p[2 * i + 1]), nw), g[2 * i], g[2 * i + 1]);
+                float ex[8];
+                exp8(x[k], row.m2, ex);
+                grad8(ex, row, g);
                 const int64_t r = y - col[k];
                 if (r >= 0 && r < 8) {
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
-                        if (e == r) g[e] = fmaf(negw, p[e], w);  // w (1 - p_y)
+                        if (e == r) g[e] = grad_label(ex[e], row);  // w (1 - p_y)
                 }
             } else {
 #pragma unroll
@@ -296,9 +291,8 @@ __global__ void __launch_bounds__(kBwdThreads)
         float g;
         if (mode == 2) {
             const float x = Elem<Ein>::to_float(zin[c]);
-            const float a = fmaf(x - M, kLog2e, -log2S);
-            const float p = ex2_approx(a);
-            g = (c == y) ? fmaf(negw, p, w) : negw * p;
+            const float e = ex2_approx(fmaf(x, kLog2e, -row.m2));
+            g = (c == y) ? grad_label(e, row) : e * row.nwK;
         } else {
             g = fill;
         }
