@@ -267,8 +267,8 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
             const uint32_t bytes = (uint32_t)tk.len * (uint32_t)sizeof(Ein);
             // pass 1: the row is read again by pass 2, so keep it in L2
             mbar_arrive_expect_tx(&bars[slot], bytes);
-            bulk_g2s_evict_first(slots + (size_t)slot * kSlotBytes, tk.src, bytes, &bars[slot],
-                                 c.pass == 0 ? pol_keep : pol_once);
+            bulk_g2s_hint(slots + (size_t)slot * kSlotBytes, tk.src, bytes, &bars[slot],
+                          c.pass == 0 ? pol_keep : pol_once);
         }
     };
 

@@ -758,17 +758,29 @@ static cudaError_t launch_transpose(const uint16_t* src, int64_t rows, int64_t c
 // A stream and events of one backward call: the W transposes run there, next
 // to the GEMMs on the caller's stream.  Created per call and released at the
 // end of it (destruction waits for nothing; the driver frees them once their
-// work is done), so concurrent calls never share them.
+// work is done), so concurrent calls never share them.  Once forked from the
+// caller's stream, the side stream is joined back into it when this object
+// goes out of scope -- on every return path, errors included -- so nothing
+// the call queued can outlive the caller's view of it.
 struct SideStream {
-    cudaStream_t s = nullptr;
+    cudaStream_t s = nullptr, caller = nullptr;
     cudaEvent_t start = nullptr, hT = nullptr, done = nullptr, tr[2] = {}, acc[2] = {};
-    bool ok = false;
+    bool ok = false, forked = false;
     SideStream() {
         ok = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) == cudaSuccess;
         for (cudaEvent_t* e : {&start, &hT, &done, &tr[0], &tr[1], &acc[0], &acc[1]})
             ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
     }
+    // The side stream's work starts after everything queued so far on `c`.
+    bool fork(cudaStream_t c) {
+        caller = c;
+        forked = cudaEventRecord(start, c) == cudaSuccess &&
+                 cudaStreamWaitEvent(s, start, 0) == cudaSuccess;
+        return forked;
+    }
     ~SideStream() {
+        if (forked && cudaEventRecord(done, s) == cudaSuccess)
+            cudaStreamWaitEvent(caller, done, 0);
         for (cudaEvent_t e : {start, hT, done, tr[0], tr[1], acc[0], acc[1]})
             if (e) cudaEventDestroy(e);
         if (s) cudaStreamDestroy(s);
@@ -945,9 +957,7 @@ int pstat_lmhead_backward(const void* hidden, const void* W, int64_t T, int64_t 
         return lm::launch_transpose(static_cast<const uint16_t*>(W) + c0 * d, vc, d, d,
                                     Wt[c & 1], lm::VC, lm::VC, dev_error, x.s);
     };
-    if (cudaEventRecord(x.start, st) != cudaSuccess ||
-        cudaStreamWaitEvent(x.s, x.start, 0) != cudaSuccess)
-        return PSTAT_ERR_CUDA;
+    if (!x.fork(st)) return PSTAT_ERR_CUDA;
     // hidden^T once (fp16, tokens padded to Tp with zeros)
     if (lm::launch_transpose(static_cast<const uint16_t*>(hidden), T, d, d, hT, Tp, Tp, dev_error,
                              x.s) != cudaSuccess ||
@@ -1003,10 +1013,7 @@ int pstat_lmhead_backward(const void* hidden, const void* W, int64_t T, int64_t 
         if (e != cudaSuccess || cudaEventRecord(x.acc[b], st) != cudaSuccess)
             return PSTAT_ERR_CUDA;
     }
-    // join: the side stream's work precedes whatever the caller queues next
-    if (cudaEventRecord(x.done, x.s) != cudaSuccess ||
-        cudaStreamWaitEvent(st, x.done, 0) != cudaSuccess)
-        return PSTAT_ERR_CUDA;
+    // x joins the side stream back into st as it goes out of scope
     return PSTAT_OK;
 }
 

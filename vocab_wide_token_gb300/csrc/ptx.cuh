@@ -70,20 +70,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 }
 
 // ---- bulk asynchronous copy (global -> shared), completion on an mbarrier --
-// Both addresses must be 16-byte aligned and `bytes` a multiple of 16.
-__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes,
-                                         uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-            "r"(smem_u32(smem_dst)),
-        "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-
-// Same, with an L2 eviction-first hint: the data are streamed once.
-__device__ __forceinline__ void bulk_g2s_evict_first(void* smem_dst, const void* gmem_src,
-                                                     uint32_t bytes, uint64_t* bar,
-                                                     uint64_t policy) {
+// Both addresses must be 16-byte aligned and `bytes` a multiple of 16.  The L2
+// cache policy comes from createpolicy: evict-first for data streamed once,
+// evict-last for data read again soon.
+__device__ __forceinline__ void bulk_g2s_hint(void* smem_dst, const void* gmem_src, uint32_t bytes,
+                                              uint64_t* bar, uint64_t policy) {
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
         "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(smem_dst)),

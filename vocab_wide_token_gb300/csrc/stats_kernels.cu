@@ -97,8 +97,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         if (locate(it, src, len) && lane == 0) {
             const uint32_t bytes = (uint32_t)len * (uint32_t)sizeof(E);
             mbar_arrive_expect_tx(&bars[slot], bytes);
-            bulk_g2s_evict_first(slots + (size_t)slot * kSlotBytes, src, bytes, &bars[slot],
-                                 policy);
+            bulk_g2s_hint(slots + (size_t)slot * kSlotBytes, src, bytes, &bars[slot], policy);
         }
     };
 
