@@ -357,7 +357,7 @@ def main():
                      "forward_ms": fwd_ms, "forward_gbs": fwd_gbs, "forward_frac": fwd_gbs / hbm,
                      "backward_ms": bwd_ms, "backward_gbs": bwd_gbs,
                      "backward_frac": bwd_gbs / hbm, "active_rows": active_rows,
-                     "gpu_launches": 3 * K},
+                     "gpu_launches": 2 * K},
         "clocks": clocks.summary(),
     }
 

@@ -114,7 +114,11 @@ PSTAT_API int pstat_workspace_size(int64_t T, int64_t V, pstat_dtype dt, const i
                          int n_shards, size_t* bytes);
 
 /*
- * Forward statistics (chunk-statistics kernel, then the fixed-order combine).
+ * Forward statistics: per-chunk statistics combined in a fixed order.  Plans
+ * of at most 256 chunks per row run as one kernel with the records in shared
+ * memory (the workspace is then not touched); larger plans run the
+ * chunk-statistics kernel into the workspace, then the combine.  Both give
+ * the same bits.
  *   logits        [T, ld] dtype `dt`; element (t, v) at logits + t*ld + v.
  *                 Any alignment works; 16-byte aligned rows and chunk starts
  *                 take the bulk-copy path, others a slower path with the same
@@ -124,7 +128,8 @@ PSTAT_API int pstat_workspace_size(int64_t T, int64_t V, pstat_dtype dt, const i
  *                 n_shards <= PSTAT_MAX_SHARDS; NULL means {0, V}.
  *   out_logprob   [T] float (may be NULL), out_entropy [T] float (may be
  *                 NULL), out_rowstats [T, 2] float (M, ln S) (may be NULL).
- *   workspace     >= pstat_workspace_size(...) bytes, 16-byte aligned.
+ *   workspace     >= pstat_workspace_size(...) bytes, 16-byte aligned
+ *                 (required either way).
  *   dev_error     device int or NULL; bits PSTAT_DEV_*.
  * T = 0 is a no-op returning PSTAT_OK.
  */

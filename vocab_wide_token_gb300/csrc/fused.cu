@@ -18,6 +18,11 @@
 // keeps in L2, and pass 2 then misses L2: measured slower.)  Every record, fold
 // and gradient element is computed by the same code as in the two-call path,
 // so the results are bit-identical to pstat_forward + pstat_backward.
+//
+// The same kernel without pass 2 is pstat_forward's one-kernel path (for
+// plans of at most 256 chunks per row): pass 1 with an evict-first hint, and
+// one designated warp folding every row, so that no warp's next row waits for
+// a fold.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -50,7 +55,8 @@ constexpr size_t kBarBytes = (size_t)kFbWarps * kFbStages * sizeof(uint64_t);
 constexpr size_t kRecOff = (kRingBytes + kBarBytes + 15) / 16 * 16;  // float4 records
 constexpr size_t kInfoOff = kRecOff + 2 * kFbMaxChunks * sizeof(float4);
 constexpr size_t kReadyOff = kInfoOff + 2 * sizeof(RowInfo);
-constexpr size_t kCountOff = kReadyOff + 2 * sizeof(uint64_t);
+constexpr size_t kRecsOff = kReadyOff + 2 * sizeof(uint64_t);  // forward only
+constexpr size_t kCountOff = kRecsOff + 2 * sizeof(uint64_t);
 // Labels and weights of the CTA's first kFbRowCache rows, loaded once at the
 // start so that the fold finds them in shared memory.
 constexpr int kFbRowCache = 384;
@@ -153,7 +159,8 @@ __device__ __forceinline__ void unpack_vec<float>(const uint4& v, float (&x)[4])
     x[3] = __uint_as_float(v.w);
 }
 
-template <typename Ein, typename Eout>
+// kBwd = false: pass 1 only (the forward: logprob, entropy, (M, ln S)).
+template <typename Ein, typename Eout, bool kBwd>
 __global__ void __launch_bounds__(kFbWarps * 32, 1)
     fwdbwd_kernel(const Ein* __restrict__ logits, int64_t T, int64_t V, int64_t ld,
                   const __grid_constant__ ShardPlan plan, const int64_t* __restrict__ labels,
@@ -170,6 +177,7 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
     float4* records = reinterpret_cast<float4*>(smem + kRecOff);
     RowInfo* info = reinterpret_cast<RowInfo*>(smem + kInfoOff);
     uint64_t* ready = reinterpret_cast<uint64_t*>(smem + kReadyOff);
+    uint64_t* recs = reinterpret_cast<uint64_t*>(smem + kRecsOff);
     int* counter = reinterpret_cast<int*>(smem + kCountOff);
     int64_t* lab_s = reinterpret_cast<int64_t*>(smem + kLabOff);
     float* wt_s = reinterpret_cast<float*>(smem + kWtOff);
@@ -182,6 +190,9 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
     if (threadIdx.x == 0) {
         mbar_init(&ready[0], 1);
         mbar_init(&ready[1], 1);
+        const int others = (nc < kFbWarps ? nc : kFbWarps) - 1;
+        mbar_init(&recs[0], others > 0 ? others : 1);
+        mbar_init(&recs[1], others > 0 ? others : 1);
         counter[0] = 0;
         counter[1] = 0;
     }
@@ -209,7 +220,8 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
     const uint64_t pol_once = policy_evict_first();
 
     // A warp's work is the sequence of segments pass 1 of row k, pass 2 of
-    // row k, for the CTA's rows k = 0, 1, ... in order.
+    // row k, for the CTA's rows k = 0, 1, ... in order (pass 1 only without
+    // the backward).
     struct Cursor {
         int64_t k;
         int pass, i, cnt, g0;
@@ -227,7 +239,7 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
             load_segment(c);
             if (c.i < c.cnt) return;
             c.i = 0;
-            if (c.pass == 0) {
+            if (c.pass == 0 && kBwd) {
                 c.pass = 1;
             } else {
                 c.pass = 0;
@@ -265,10 +277,10 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
         if (tk.bulk && lane == 0) {
             const int slot = (int)(pos % kFbStages);
             const uint32_t bytes = (uint32_t)tk.len * (uint32_t)sizeof(Ein);
-            // pass 1: the row is read again by pass 2, so keep it in L2
+            // pass 1 of the single pass: the row is read again by pass 2, so keep it in L2
             mbar_arrive_expect_tx(&bars[slot], bytes);
             bulk_g2s_hint(slots + (size_t)slot * kSlotBytes, tk.src, bytes, &bars[slot],
-                          c.pass == 0 ? pol_keep : pol_once);
+                          (kBwd && c.pass == 0) ? pol_keep : pol_once);
         }
     };
 
@@ -294,7 +306,18 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
         const int len = tk.len;
         const int64_t start = tk.start;
 
-        if (cc.pass == 1 && cc.i == 0) {
+        if (!kBwd && cc.i == 0 && tk.r >= 2) {
+            // Forward only: the records, counter and row slot of parity b are
+            // reused once row r - 2 is folded (nothing else holds warps within
+            // a row of each other).
+            bool ok = mbar_wait_bounded(&ready[b], (uint32_t)(((tk.r - 2) >> 1) & 1), kWaitLimitNs);
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            if (!ok) {
+                failed = true;
+                break;
+            }
+        }
+        if (kBwd && cc.pass == 1 && cc.i == 0) {
             // (M, ln S) of this row, published by the warp that folded it.
             bool ok = mbar_wait_bounded(&ready[b], (uint32_t)((tk.r >> 1) & 1), kWaitLimitNs);
             ok = __all_sync(0xFFFFFFFFu, ok);
@@ -335,15 +358,36 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
             const float4 rec = reduce_regs(q, (Ein*)nullptr);
             if (lane == 0) records[b * kFbMaxChunks + tk.g] = rec;
             if (cc.i == cc.cnt - 1) {
-                // This warp's last chunk of the row: the last warp to get here folds.
+                // This warp's last chunk of the row.  With the backward, every
+                // warp waits for the fold anyway, so the last warp to get here
+                // folds.  Forward only, nobody waits for it, and the folding
+                // warp would start its next row late every row: warp active-1,
+                // which has the fewest chunks per row, folds every row once
+                // the others' records are in.
                 __syncwarp();
-                int arrived = 0;
-                if (lane == 0) {
-                    __threadfence_block();
-                    arrived = atomicAdd(&counter[b], 1);
+                bool fold_now;
+                if constexpr (kBwd) {
+                    int arrived = 0;
+                    if (lane == 0) {
+                        __threadfence_block();
+                        arrived = atomicAdd(&counter[b], 1);
+                    }
+                    arrived = __shfl_sync(0xFFFFFFFFu, arrived, 0);
+                    fold_now = arrived == active - 1;
+                } else if (warp != active - 1) {
+                    if (lane == 0) mbar_arrive(&recs[b]);  // release: this warp's records
+                    fold_now = false;
+                } else {
+                    bool ok = active == 1 ||
+                              mbar_wait_bounded(&recs[b], (uint32_t)((tk.r >> 1) & 1), kWaitLimitNs);
+                    ok = __all_sync(0xFFFFFFFFu, ok);
+                    if (!ok) {
+                        failed = true;
+                        break;
+                    }
+                    fold_now = true;
                 }
-                arrived = __shfl_sync(0xFFFFFFFFu, arrived, 0);
-                if (arrived == active - 1) {
+                if (fold_now) {
                     __threadfence_block();
                     // Label, weight and z_y first: the z_y load then runs
                     // under the fold's arithmetic.
@@ -398,7 +442,7 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
                 }
                 __syncwarp();
             }
-        } else {
+        } else if constexpr (kBwd) {
             // dlogits of this chunk: columns [start, start + len) of row t
             Eout* dst = out + tk.t * ld_out + start;
             const int64_t y = ri.y;
@@ -475,7 +519,7 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
     }
 }
 
-template <typename Ein, typename Eout>
+template <typename Ein, typename Eout, bool kBwd>
 cudaError_t launch_fused_t(const Ein* logits, int64_t T, int64_t V, int64_t ld,
                            const ShardPlan& plan, const int64_t* labels, int64_t ignore_index,
                            const float* weights, float* logprob, float* entropy, float* rowstats,
@@ -485,20 +529,38 @@ cudaError_t launch_fused_t(const Ein* logits, int64_t T, int64_t V, int64_t ld,
     int d = 0;
     cudaGetDevice(&d);
     if (d >= 64 || !configured[d].load(std::memory_order_acquire)) {
-        const cudaError_t e = cudaFuncSetAttribute(fwdbwd_kernel<Ein, Eout>,
+        const cudaError_t e = cudaFuncSetAttribute(fwdbwd_kernel<Ein, Eout, kBwd>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    (int)kFusedSmem);
         if (e != cudaSuccess) return e;
         if (d < 64) configured[d].store(true, std::memory_order_release);
     }
     const int64_t grid = T < dev.sm_count ? T : dev.sm_count;
-    fwdbwd_kernel<Ein, Eout><<<(unsigned)grid, kFbWarps * 32, kFusedSmem, stream>>>(
+    fwdbwd_kernel<Ein, Eout, kBwd><<<(unsigned)grid, kFbWarps * 32, kFusedSmem, stream>>>(
         logits, T, V, ld, plan, labels, ignore_index, weights, logprob, entropy, rowstats, out,
         ld_out, dev_error);
     return cudaGetLastError();
 }
 
 }  // namespace
+
+int forward_rows_max_chunks() { return kFbMaxChunks; }
+
+cudaError_t launch_forward_rows(const void* logits, pstat_dtype dt, int64_t T, int64_t V,
+                                int64_t ld, const ShardPlan& plan, const int64_t* labels,
+                                int64_t ignore_index, float* logprob, float* entropy,
+                                float* rowstats, int* dev_error, const DeviceInfo& dev,
+                                cudaStream_t stream) {
+    if (plan.n_chunks > kFbMaxChunks) return cudaErrorInvalidValue;
+    if (dt == PSTAT_BF16)
+        return launch_fused_t<uint16_t, float, false>(
+            static_cast<const uint16_t*>(logits), T, V, ld, plan, labels, ignore_index, nullptr,
+            logprob, entropy, rowstats, nullptr, 0, dev_error, dev, stream);
+    return launch_fused_t<float, float, false>(static_cast<const float*>(logits), T, V, ld, plan,
+                                               labels, ignore_index, nullptr, logprob, entropy,
+                                               rowstats, nullptr, 0, dev_error, dev, stream);
+}
+
 }  // namespace pstat
 
 using namespace pstat;
@@ -534,16 +596,16 @@ extern "C" int pstat_forward_backward(const void* logits, pstat_dtype dt, int64_
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (dt == PSTAT_BF16)
-        e = launch_fused_t(static_cast<const uint16_t*>(logits), T, V, ld, plan, labels,
-                           ignore_index, weights, out_logprob, out_entropy, out_rowstats,
+        e = launch_fused_t<uint16_t, uint16_t, true>(static_cast<const uint16_t*>(logits), T, V,
+                           ld, plan, labels, ignore_index, weights, out_logprob, out_entropy, out_rowstats,
                            static_cast<uint16_t*>(out_dlogits), ld_out, dev_error, dev, st);
     else if (out_dt == PSTAT_BF16)
-        e = launch_fused_t(static_cast<const float*>(logits), T, V, ld, plan, labels,
-                           ignore_index, weights, out_logprob, out_entropy, out_rowstats,
+        e = launch_fused_t<float, uint16_t, true>(static_cast<const float*>(logits), T, V, ld,
+                           plan, labels, ignore_index, weights, out_logprob, out_entropy, out_rowstats,
                            static_cast<uint16_t*>(out_dlogits), ld_out, dev_error, dev, st);
     else
-        e = launch_fused_t(static_cast<const float*>(logits), T, V, ld, plan, labels,
-                           ignore_index, weights, out_logprob, out_entropy, out_rowstats,
+        e = launch_fused_t<float, float, true>(static_cast<const float*>(logits), T, V, ld,
+                           plan, labels, ignore_index, weights, out_logprob, out_entropy, out_rowstats,
                            static_cast<float*>(out_dlogits), ld_out, dev_error, dev, st);
     return e == cudaSuccess ? PSTAT_OK : PSTAT_ERR_CUDA;
 }

@@ -62,4 +62,16 @@ cudaError_t launch_logsoftmax(const void* logits, pstat_dtype dt, int64_t T, int
                               const float* rowstats, void* out, pstat_dtype out_dt, int64_t ld_out,
                               int* dev_error, cudaStream_t stream);
 
+// The forward in one kernel (fused.cu): the single-pass kernel's first pass,
+// chunk records in shared memory, each row folded by the warp that finishes
+// it; the same records, fold and outputs as launch_chunk_stats + launch_combine,
+// bit for bit.  Plans with more than forward_rows_max_chunks() chunks per row
+// return cudaErrorInvalidValue without launching.
+int forward_rows_max_chunks();
+cudaError_t launch_forward_rows(const void* logits, pstat_dtype dt, int64_t T, int64_t V,
+                                int64_t ld, const ShardPlan& plan, const int64_t* labels,
+                                int64_t ignore_index, float* logprob, float* entropy,
+                                float* rowstats, int* dev_error, const DeviceInfo& dev,
+                                cudaStream_t stream);
+
 }  // namespace pstat

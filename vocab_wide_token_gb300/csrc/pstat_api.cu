@@ -139,6 +139,13 @@ int pstat_forward(const void* logits, pstat_dtype dt, int64_t T, int64_t V, int6
     rc = device_info(&dev);
     if (rc != PSTAT_OK) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (plan.n_chunks <= forward_rows_max_chunks()) {
+        // one kernel; the workspace is not touched
+        return launch_forward_rows(logits, dt, T, V, ld, plan, labels, ignore_index, out_logprob,
+                                   out_entropy, out_rowstats, dev_error, dev, st) == cudaSuccess
+                   ? PSTAT_OK
+                   : PSTAT_ERR_CUDA;
+    }
     float4* cs = reinterpret_cast<float4*>(static_cast<char*>(workspace) + wl.chunk_stats_off);
     if (launch_chunk_stats(logits, dt, T, ld, plan, cs, dev_error, dev, st) != cudaSuccess)
         return PSTAT_ERR_CUDA;
