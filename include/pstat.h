@@ -209,6 +209,69 @@ PSTAT_API int pstat_forward_backward(const void* logits, pstat_dtype dt, int64_t
                                      int64_t ld_out, int* dev_error, pstat_stream_t stream);
 
 /*
+ * Vocabulary-parallel use: each rank holds the logits of one vocabulary shard
+ * [b_s, b_{s+1}) of every row (torchtitan PR #4685, Summary and the review
+ * thread's batch-invariance answer: shard-local maximum, sum of exponentials,
+ * entropy-weighted sum and target logit, reduced across ranks).  Here the
+ * ranks exchange the [T, 4] statistics with an all-gather instead of MAX/SUM
+ * all-reduces, and every rank folds them in ascending shard order with
+ * pstat_combine_shards, so all ranks hold the same bits and the result does
+ * not depend on the collective's reduction order.
+ *
+ * pstat_shard_stats on every shard followed by pstat_combine_shards equals
+ * pstat_forward with those shard_bounds bit for bit; pstat_backward_shard
+ * equals the shard's columns of pstat_backward.
+ */
+
+/*
+ * Per-row statistics of one vocabulary shard.
+ *   logits        [T, ld] dtype `dt`: this shard's V columns (chunks are laid
+ *                 from its first column).  V may hold at most 256 chunks
+ *                 (PSTAT_ERR_SHAPE otherwise).
+ *   labels        [T] int64 in the whole vocabulary's numbering, or NULL.
+ *   vocab_start   the shard's first column in that numbering (b_s).
+ *   out_stats     [T, 4] float, 16-byte aligned: (M_s, S_s, U_s, z_y) with
+ *                 S_s = sum exp(z - M_s), U_s = sum exp(z - M_s)(z - M_s) over
+ *                 the shard, and z_y the label's logit when vocab_start <= y <
+ *                 vocab_start + V, else 0.  A fully masked shard gives
+ *                 (-inf, 0, 0, .).  Label range errors are reported by
+ *                 pstat_combine_shards.
+ */
+PSTAT_API int pstat_shard_stats(const void* logits, pstat_dtype dt, int64_t T, int64_t V,
+                                int64_t ld, const int64_t* labels, int64_t ignore_index,
+                                int64_t vocab_start, float* out_stats, int* dev_error,
+                                pstat_stream_t stream);
+
+/*
+ * Fixed-order combine of gathered shard statistics into the row outputs.
+ *   stats         [T, n_shards, 4] float (device, 16-byte aligned): row t,
+ *                 shard s at stats + (t n_shards + s) 4, shards in ascending
+ *                 vocabulary order.
+ *   shard_bounds  host int64[n_shards + 1], 0 = b_0 < ... < b_S = V_total.
+ *   Outputs, labels and dev_error as pstat_forward (bad labels: bit 1, NaN;
+ *   fully masked rows: bit 2, NaN).
+ */
+PSTAT_API int pstat_combine_shards(const float* stats, int64_t T, int n_shards,
+                                   const int64_t* shard_bounds, const int64_t* labels,
+                                   int64_t ignore_index, float* out_logprob, float* out_entropy,
+                                   float* out_rowstats, int* dev_error, pstat_stream_t stream);
+
+/*
+ * Weighted backward of one vocabulary shard's columns.
+ *   As pstat_backward on the shard's V columns, with rowstats [T, 2] the
+ *   global (M, ln S) (required) and labels in the whole vocabulary's
+ *   numbering: the one-hot term lands in this shard only when vocab_start <=
+ *   y < vocab_start + V; labels outside [0, vocab_total) give NaN rows and
+ *   dev_error bit 1.  vocab_start + V <= vocab_total.
+ */
+PSTAT_API int pstat_backward_shard(const void* logits, pstat_dtype dt, int64_t T, int64_t V,
+                                   int64_t ld, const int64_t* labels, int64_t ignore_index,
+                                   const float* weights, const float* rowstats,
+                                   int64_t vocab_start, int64_t vocab_total, void* out_dlogits,
+                                   pstat_dtype out_dt, int64_t ld_out, int* dev_error,
+                                   pstat_stream_t stream);
+
+/*
  * The full log-softmax log p_tv = z_tv - M_t - ln S_t as a [T, V] tensor, in
  * one read and one write pass over the logits, from the same row statistics
  * as the other entry points (so it is batch-invariant too: a row's output

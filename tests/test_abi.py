@@ -154,3 +154,40 @@ def test_lmhead_argument_checks(lib):
     assert bw(dW=0x7004) == -5
     assert bw(ws_bytes=16) == -6
     assert bw(ws=0x8010) == -5         # 1024-byte aligned workspace
+
+
+def test_shard_entry_argument_checks(lib):
+    c = ctypes.c_void_p
+    # pstat_shard_stats(logits, dt, T, V, ld, labels, ignore, vocab_start, out, dev_error, stream)
+    def stats(dt=1, T=4, V=100, ld=100, start=0, logits=0x1000, out=0x2000):
+        return lib.pstat_shard_stats(c(logits), dt, T, V, ld, None, -100, start, c(out), None,
+                                     None)
+    assert stats(dt=7) == -4
+    assert stats(V=0) == -2
+    assert stats(ld=50) == -2
+    assert stats(start=-1) == -2
+    assert stats(V=256 * 4096 + 1, ld=256 * 4096 + 1) == -2  # more than 256 chunks
+    assert stats(T=0) == 0
+    assert stats(out=0) == -1
+    assert stats(out=0x2008) == -5                             # float4 output: 16-byte aligned
+    # pstat_combine_shards(stats, T, n_shards, bounds, labels, ignore, lp, ent, rs, err, stream)
+    def comb(bounds, n=None, T=4, st=0x3000):
+        b = (ctypes.c_int64 * len(bounds))(*bounds)
+        n = len(bounds) - 1 if n is None else n
+        return lib.pstat_combine_shards(c(st), T, n, b, None, -100, None, None, None, None,
+                                        None)
+    assert comb([0, 10, 5]) == -3
+    assert comb([1, 10]) == -3
+    assert comb([0, 10], n=0) == -3
+    assert comb([0, 10], T=-1) == -2
+    assert comb([0, 10], T=0) == 0
+    assert comb([0, 10], st=0) == -1
+    assert comb([0, 10], st=0x3004) == -5
+    # pstat_backward_shard(logits, dt, T, V, ld, labels, ignore, w, rs, start, total, out,
+    #                      out_dt, ld_out, err, stream)
+    def bwd(dt=1, out_dt=1, V=100, start=0, total=100, rs=0x4000):
+        return lib.pstat_backward_shard(c(0x1000), dt, 4, V, V, None, -100, None, c(rs), start,
+                                        total, c(0x5000), out_dt, V, None, None)
+    assert bwd(dt=1, out_dt=0) == -4
+    assert bwd(start=50, total=120) == -2
+    assert bwd(rs=0) == -1

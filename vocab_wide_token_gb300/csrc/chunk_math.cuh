@@ -248,6 +248,17 @@ __device__ __forceinline__ void load_chunk_regs(const void* buf, int len, int la
 // skipped.  The order depends only on the shard plan, and every lane ends
 // with the same (M, S, U).
 // ---------------------------------------------------------------------------
+// Moves one shard's sums (ps, pu), relative to its maximum Ms, onto the row
+// maximum M and adds them to the running row sums (S, U).  Shards are taken in
+// ascending order; a shard whose maximum is -inf is skipped by the caller.
+__device__ __forceinline__ void fold_shard(float Ms, float ps, float pu, float M, float& S,
+                                           float& U) {
+    const float dM = Ms - M;
+    const float f = expf(dM);
+    S = fmaf(ps, f, S);
+    U = fmaf(f, fmaf(dM, ps, pu), U);
+}
+
 __device__ __forceinline__ float3 fold_row_warp(const float4* rec, const ShardPlan& plan,
                                                 int lane) {
     float M = -INFINITY;
@@ -275,10 +286,7 @@ __device__ __forceinline__ float3 fold_row_warp(const float4* rec, const ShardPl
                 ps += __shfl_xor_sync(0xFFFFFFFFu, ps, off);
                 pu += __shfl_xor_sync(0xFFFFFFFFu, pu, off);
             }
-            const float dM = Ms - M;
-            const float f = expf(dM);
-            S = fmaf(ps, f, S);
-            U = fmaf(f, fmaf(dM, ps, pu), U);
+            fold_shard(Ms, ps, pu, M, S, U);
         }
     }
     return make_float3(M, S, U);

@@ -167,7 +167,12 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
                   int64_t ignore_index, const float* __restrict__ weights,
                   float* __restrict__ logprob, float* __restrict__ entropy,
                   float* __restrict__ rowstats, Eout* __restrict__ out, int64_t ld_out,
+                  float4* __restrict__ shard_out, int64_t label_offset,
                   int* __restrict__ dev_error) {
+    // shard_out (forward only): instead of the row outputs, write the row's
+    // statistics (M, S, U, z_y) for this vocabulary shard, whose first column
+    // is label_offset in the labels' numbering; z_y is 0 when the label lies
+    // outside the shard.
     constexpr int kVec = Elem<Ein>::kVec;
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5;
@@ -395,11 +400,15 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
                     const bool cached = tk.r < kFbRowCache;
                     const int64_t y = cached ? lab_s[tk.r] : (labels ? labels[t] : ignore_index);
                     const float w = cached ? wt_s[tk.r] : (weights ? weights[t] : 1.f);
-                    const bool y_in = y != ignore_index && y >= 0 && y < V;
+                    const int64_t yl = y - label_offset;  // the label's column here
+                    const bool y_in = y != ignore_index && yl >= 0 && yl < V;
                     float zy = 0.f;
-                    if (lane == 0 && y_in) zy = Elem<Ein>::to_float(logits[t * ld + y]);
+                    if (lane == 0 && y_in) zy = Elem<Ein>::to_float(logits[t * ld + yl]);
                     const float3 st = fold_row_warp(records + b * kFbMaxChunks, plan, lane);
-                    if (lane == 0) {
+                    if (lane == 0 && shard_out) {
+                        shard_out[t] = make_float4(st.x, st.y, st.z, zy);
+                        mbar_arrive(&ready[b]);
+                    } else if (lane == 0) {
                         counter[b] = 0;
                         const float M = st.x, S = st.y, U = st.z;
                         int err = 0;
@@ -524,7 +533,8 @@ cudaError_t launch_fused_t(const Ein* logits, int64_t T, int64_t V, int64_t ld,
                            const ShardPlan& plan, const int64_t* labels, int64_t ignore_index,
                            const float* weights, float* logprob, float* entropy, float* rowstats,
                            Eout* out, int64_t ld_out, int* dev_error, const DeviceInfo& dev,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, float4* shard_out = nullptr,
+                           int64_t label_offset = 0) {
     static std::atomic<bool> configured[64];
     int d = 0;
     cudaGetDevice(&d);
@@ -538,7 +548,7 @@ cudaError_t launch_fused_t(const Ein* logits, int64_t T, int64_t V, int64_t ld,
     const int64_t grid = T < dev.sm_count ? T : dev.sm_count;
     fwdbwd_kernel<Ein, Eout, kBwd><<<(unsigned)grid, kFbWarps * 32, kFusedSmem, stream>>>(
         logits, T, V, ld, plan, labels, ignore_index, weights, logprob, entropy, rowstats, out,
-        ld_out, dev_error);
+        ld_out, shard_out, label_offset, dev_error);
     return cudaGetLastError();
 }
 
@@ -550,15 +560,17 @@ cudaError_t launch_forward_rows(const void* logits, pstat_dtype dt, int64_t T, i
                                 int64_t ld, const ShardPlan& plan, const int64_t* labels,
                                 int64_t ignore_index, float* logprob, float* entropy,
                                 float* rowstats, int* dev_error, const DeviceInfo& dev,
-                                cudaStream_t stream) {
+                                cudaStream_t stream, float4* shard_out, int64_t label_offset) {
     if (plan.n_chunks > kFbMaxChunks) return cudaErrorInvalidValue;
     if (dt == PSTAT_BF16)
         return launch_fused_t<uint16_t, float, false>(
             static_cast<const uint16_t*>(logits), T, V, ld, plan, labels, ignore_index, nullptr,
-            logprob, entropy, rowstats, nullptr, 0, dev_error, dev, stream);
+            logprob, entropy, rowstats, nullptr, 0, dev_error, dev, stream, shard_out,
+            label_offset);
     return launch_fused_t<float, float, false>(static_cast<const float*>(logits), T, V, ld, plan,
                                                labels, ignore_index, nullptr, logprob, entropy,
-                                               rowstats, nullptr, 0, dev_error, dev, stream);
+                                               rowstats, nullptr, 0, dev_error, dev, stream,
+                                               shard_out, label_offset);
 }
 
 }  // namespace pstat

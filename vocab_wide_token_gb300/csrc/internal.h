@@ -56,7 +56,8 @@ cudaError_t launch_backward(const void* logits, pstat_dtype dt, int64_t T, int64
                             int64_t ld, const int64_t* labels, int64_t ignore_index,
                             const float* weights, const float* rowstats, void* out,
                             pstat_dtype out_dt, int64_t ld_out, int* dev_error,
-                            const DeviceInfo& dev, cudaStream_t stream);
+                            const DeviceInfo& dev, cudaStream_t stream,
+                            int64_t label_offset = 0, int64_t v_total = -1);
 
 cudaError_t launch_logsoftmax(const void* logits, pstat_dtype dt, int64_t T, int64_t V, int64_t ld,
                               const float* rowstats, void* out, pstat_dtype out_dt, int64_t ld_out,
@@ -66,12 +67,15 @@ cudaError_t launch_logsoftmax(const void* logits, pstat_dtype dt, int64_t T, int
 // chunk records in shared memory, each row folded by the warp that finishes
 // it; the same records, fold and outputs as launch_chunk_stats + launch_combine,
 // bit for bit.  Plans with more than forward_rows_max_chunks() chunks per row
-// return cudaErrorInvalidValue without launching.
+// return cudaErrorInvalidValue without launching.  With shard_out the kernel
+// writes each row's (M, S, U, z_y) for a vocabulary shard instead of the row
+// outputs (labels numbered from label_offset; z_y = 0 off the shard).
 int forward_rows_max_chunks();
 cudaError_t launch_forward_rows(const void* logits, pstat_dtype dt, int64_t T, int64_t V,
                                 int64_t ld, const ShardPlan& plan, const int64_t* labels,
                                 int64_t ignore_index, float* logprob, float* entropy,
                                 float* rowstats, int* dev_error, const DeviceInfo& dev,
-                                cudaStream_t stream);
+                                cudaStream_t stream, float4* shard_out = nullptr,
+                                int64_t label_offset = 0);
 
 }  // namespace pstat

@@ -224,7 +224,10 @@ __global__ void __launch_bounds__(kBwdThreads)
     backward_kernel(const Ein* __restrict__ logits, int64_t V, int64_t ld,
                     const int64_t* __restrict__ labels, int64_t ignore_index,
                     const float* __restrict__ weights, const float2* __restrict__ rowstats,
-                    Eout* __restrict__ out, int64_t ld_out, int segs, int* __restrict__ dev_error) {
+                    Eout* __restrict__ out, int64_t ld_out, int segs, int64_t label_offset,
+                    int64_t v_total, int* __restrict__ dev_error) {
+    // The columns are [label_offset, label_offset + V) of a vocabulary of
+    // v_total (the whole row: 0 and V); labels are checked against v_total.
     const int64_t t = blockIdx.x / segs;
     const int seg = (int)(blockIdx.x - t * segs);
     const int64_t nv_row = V >> 3;  // whole 8-element groups in the row
@@ -234,6 +237,7 @@ __global__ void __launch_bounds__(kBwdThreads)
     Eout* zout = out + t * ld_out;
 
     const int64_t y = labels ? labels[t] : ignore_index;
+    const int64_t yl = y - label_offset;  // the label's column in this block of columns
     const float w = weights ? weights[t] : 1.f;
     int mode;  // 0: zero row, 1: NaN row, 2: compute
     GradRow row = {0.f, 0.f, 0.f, 0.f};
@@ -241,10 +245,11 @@ __global__ void __launch_bounds__(kBwdThreads)
         mode = 0;
     } else {
         const float2 rs = rowstats[t];
-        if (y < 0 || y >= V || !(rs.x > -INFINITY) || !(rs.y == rs.y)) {
+        if (y < 0 || y >= v_total || !(rs.x > -INFINITY) || !(rs.y == rs.y)) {
             mode = 1;
             if (seg == 0 && threadIdx.x == 0 && dev_error)
-                atomicOr(dev_error, (y < 0 || y >= V) ? PSTAT_DEV_BAD_LABEL : PSTAT_DEV_EMPTY_ROW);
+                atomicOr(dev_error,
+                         (y < 0 || y >= v_total) ? PSTAT_DEV_BAD_LABEL : PSTAT_DEV_EMPTY_ROW);
         } else {
             mode = 2;
             row = grad_row(rs.x, rs.y, w);
@@ -272,7 +277,7 @@ __global__ void __launch_bounds__(kBwdThreads)
                 float ex[8];
                 exp8(x[k], row.m2, ex);
                 grad8(ex, row, g);
-                const int64_t r = y - col[k];
+                const int64_t r = yl - col[k];
                 if (r >= 0 && r < 8) {
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
@@ -291,7 +296,7 @@ __global__ void __launch_bounds__(kBwdThreads)
         if (mode == 2) {
             const float x = Elem<Ein>::to_float(zin[c]);
             const float e = ex2_approx(fmaf(x, kLog2e, -row.m2));
-            g = (c == y) ? grad_label(e, row) : e * row.nwK;
+            g = (c == yl) ? grad_label(e, row) : e * row.nwK;
         } else {
             g = fill;
         }
@@ -407,7 +412,8 @@ template <typename Ein, typename Eout>
 static void launch_backward_t(const Ein* logits, int64_t T, int64_t V, int64_t ld,
                               const int64_t* labels, int64_t ignore_index, const float* weights,
                               const float* rowstats, Eout* out, int64_t ld_out, int* dev_error,
-                              const DeviceInfo& dev, cudaStream_t stream) {
+                              const DeviceInfo& dev, cudaStream_t stream, int64_t label_offset,
+                              int64_t v_total) {
     // Segments per row: enough CTAs to fill the GPU many times over, each
     // streaming at least ~32K elements.
     int64_t segs = V / 32768;
@@ -416,7 +422,7 @@ static void launch_backward_t(const Ein* logits, int64_t T, int64_t V, int64_t l
     const int64_t grid = T * segs;
     backward_kernel<Ein, Eout><<<(unsigned)grid, kBwdThreads, 0, stream>>>(
         logits, V, ld, labels, ignore_index, weights, reinterpret_cast<const float2*>(rowstats),
-        out, ld_out, (int)segs, dev_error);
+        out, ld_out, (int)segs, label_offset, v_total, dev_error);
     (void)dev;
 }
 
@@ -424,19 +430,21 @@ cudaError_t launch_backward(const void* logits, pstat_dtype dt, int64_t T, int64
                             int64_t ld, const int64_t* labels, int64_t ignore_index,
                             const float* weights, const float* rowstats, void* out,
                             pstat_dtype out_dt, int64_t ld_out, int* dev_error,
-                            const DeviceInfo& dev, cudaStream_t stream) {
+                            const DeviceInfo& dev, cudaStream_t stream, int64_t label_offset,
+                            int64_t v_total) {
+    if (v_total < 0) v_total = V;
     if (dt == PSTAT_BF16 && out_dt == PSTAT_BF16)
         launch_backward_t(static_cast<const uint16_t*>(logits), T, V, ld, labels, ignore_index,
                           weights, rowstats, static_cast<uint16_t*>(out), ld_out, dev_error, dev,
-                          stream);
+                          stream, label_offset, v_total);
     else if (dt == PSTAT_F32 && out_dt == PSTAT_BF16)
         launch_backward_t(static_cast<const float*>(logits), T, V, ld, labels, ignore_index,
                           weights, rowstats, static_cast<uint16_t*>(out), ld_out, dev_error, dev,
-                          stream);
+                          stream, label_offset, v_total);
     else
         launch_backward_t(static_cast<const float*>(logits), T, V, ld, labels, ignore_index,
                           weights, rowstats, static_cast<float*>(out), ld_out, dev_error, dev,
-                          stream);
+                          stream, label_offset, v_total);
     return cudaGetLastError();
 }
 

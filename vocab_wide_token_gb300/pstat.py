@@ -59,6 +59,13 @@ _lib.pstat_lmhead_fused.restype = _i32
 _lib.pstat_lmhead_backward.argtypes = [_vp, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _vp,
                                        _vp, _sz, _vp, _vp]
 _lib.pstat_lmhead_backward.restype = _i32
+_lib.pstat_shard_stats.argtypes = [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _vp, _vp]
+_lib.pstat_shard_stats.restype = _i32
+_lib.pstat_combine_shards.argtypes = [_vp, _i64, _i32, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp]
+_lib.pstat_combine_shards.restype = _i32
+_lib.pstat_backward_shard.argtypes = [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _i64,
+                                      _i64, _vp, _i32, _i64, _vp, _vp]
+_lib.pstat_backward_shard.restype = _i32
 
 F32, BF16 = 0, 1
 OK = 0
@@ -265,6 +272,78 @@ def forward_backward(logits: torch.Tensor, labels: torch.Tensor | None,
                                        _ptr(dev_error), _stream(dev)),
            "pstat_forward_backward")
     return lp, ent, rs, dlogits
+
+
+# ---- vocabulary-parallel use ---------------------------------------------------
+# Each rank holds one vocabulary shard [b_s, b_{s+1}) of every row.  The ranks
+# all-gather the [T, 4] shard statistics and fold them in ascending shard
+# order, so every rank gets the same bits whatever the collective's algorithm.
+
+def shard_stats(logits: torch.Tensor, labels: torch.Tensor | None, vocab_start: int,
+                ignore_index: int = -100, *, out=None, dev_error=None):
+    """(M_s, S_s, U_s, z_y) of this vocabulary shard per row, [T, 4] float32;
+    labels in the whole vocabulary's numbering (z_y = 0 off the shard)."""
+    T, V, ld = _rows(logits)
+    dev = logits.device
+    lab = _labels(labels, T, dev)
+    if out is None:
+        out = torch.empty(T, 4, dtype=torch.float32, device=dev)
+    if out.shape != (T, 4) or not out.is_contiguous() or out.dtype != torch.float32:
+        raise ValueError("out must be a contiguous float32 [T, 4] tensor")
+    _check(_lib.pstat_shard_stats(_ptr(logits), _dtype_code(logits), T, V, ld, _ptr(lab),
+                                  int(ignore_index), int(vocab_start), _ptr(out),
+                                  _ptr(dev_error), _stream(dev)), "pstat_shard_stats")
+    return out
+
+
+def combine_shards(stats: torch.Tensor, labels: torch.Tensor | None, shard_bounds,
+                   ignore_index: int = -100, *, out=None, dev_error=None):
+    """Row outputs (logprob, entropy, rowstats) from gathered shard statistics
+    stats [T, n_shards, 4], shards in ascending vocabulary order, bounds
+    shard_bounds (n_shards + 1 ints from 0 to the vocabulary size)."""
+    if stats.dim() != 3 or stats.shape[2] != 4 or stats.dtype != torch.float32:
+        raise ValueError("stats must be float32 [T, n_shards, 4]")
+    stats = stats.contiguous()
+    T, ns = stats.shape[0], stats.shape[1]
+    dev = stats.device
+    arr, nb = _bounds(shard_bounds, None)
+    if nb != ns:
+        raise ValueError("shard_bounds must have n_shards + 1 entries")
+    lab = _labels(labels, T, dev)
+    if out is None:
+        out = (torch.empty(T, dtype=torch.float32, device=dev),
+               torch.empty(T, dtype=torch.float32, device=dev),
+               torch.empty(T, 2, dtype=torch.float32, device=dev))
+    lp, ent, rs = out
+    _check(_lib.pstat_combine_shards(_ptr(stats), T, ns, arr, _ptr(lab), int(ignore_index),
+                                     _ptr(lp), _ptr(ent), _ptr(rs), _ptr(dev_error),
+                                     _stream(dev)), "pstat_combine_shards")
+    return lp, ent, rs
+
+
+def backward_shard(logits: torch.Tensor, labels: torch.Tensor | None,
+                   weights: torch.Tensor | None, rowstats: torch.Tensor, vocab_start: int,
+                   vocab_total: int, ignore_index: int = -100,
+                   out_dtype: torch.dtype | None = None, *, out=None, dev_error=None):
+    """dlogits of this vocabulary shard's columns from the global (M, ln S)."""
+    T, V, ld = _rows(logits)
+    dev = logits.device
+    lab = _labels(labels, T, dev)
+    out_dtype = out_dtype or logits.dtype
+    if out is None:
+        out = torch.empty(T, V, dtype=out_dtype, device=dev)
+    if out.dim() != 2 or out.shape != (T, V) or out.stride(1) != 1:
+        raise ValueError("out must be [T, V] with contiguous rows")
+    ld_out = out.stride(0) if T > 1 else V
+    w = None if weights is None else weights.contiguous()
+    if w is not None and (w.dtype != torch.float32 or w.shape != (T,)):
+        raise ValueError("weights must be float32 [T]")
+    _check(_lib.pstat_backward_shard(_ptr(logits), _dtype_code(logits), T, V, ld, _ptr(lab),
+                                     int(ignore_index), _ptr(w), _ptr(rowstats.contiguous()),
+                                     int(vocab_start), int(vocab_total), _ptr(out),
+                                     _dtype_code(out), ld_out, _ptr(dev_error), _stream(dev)),
+           "pstat_backward_shard")
+    return out
 
 
 _side_streams: dict = {}
