@@ -189,3 +189,25 @@ def test_autograd_function(cuda_lib):
     ref = oracle.backward(to_oracle(z.detach()), y.cpu().numpy(), adv.double().cpu().numpy(), IGN)
     assert_grad_close(z.grad, ref, torch.float32, "autograd")
     assert not ent.requires_grad
+
+
+def test_forward_past_256_chunks(cuda_lib):
+    # More than 256 chunks per row: pstat_forward takes the chunk-statistics
+    # kernel and the combine (the one-kernel path holds 256 records per row),
+    # the backward's recompute does the same, and the single pass refuses.
+    V = 256 * 4096 + 1000
+    T = 6
+    g = torch.Generator(device="cuda").manual_seed(257)
+    z = (2.0 * torch.randn(T, V, generator=g, device="cuda")).to(torch.bfloat16)
+    y = torch.randint(0, V, (T,), generator=g, device="cuda")
+    y[2] = IGN
+    w = torch.randn(T, generator=g, device="cuda")
+    lp, ent, rs = cuda_lib.forward(z, y, IGN)
+    g1 = cuda_lib.backward(z, y, w, rs, IGN)
+    g2 = cuda_lib.backward(z, y, w, None, IGN)
+    torch.cuda.synchronize()
+    assert torch.equal(g1.view(torch.int16), g2.view(torch.int16))
+    ref = oracle.forward(to_oracle(z), y.cpu().numpy(), IGN)
+    assert_forward_close(lp, ent, ref, torch.bfloat16, what="V > 256 chunks")
+    with pytest.raises(cuda_lib.PstatError):
+        cuda_lib.forward_backward(z, y, w, IGN)

@@ -251,6 +251,10 @@ __device__ __forceinline__ void load_chunk_regs(const void* buf, int len, int la
 // Moves one shard's sums (ps, pu), relative to its maximum Ms, onto the row
 // maximum M and adds them to the running row sums (S, U).  Shards are taken in
 // ascending order; a shard whose maximum is -inf is skipped by the caller.
+// This is the cross-shard step of fold_row_warp, which writes the same
+// operations out in place (as a call there the compiler schedules the
+// single-pass kernel's hot loop measurably worse); the two must stay
+// identical, and the vocabulary-parallel tests compare their bits.
 __device__ __forceinline__ void fold_shard(float Ms, float ps, float pu, float M, float& S,
                                            float& U) {
     const float dM = Ms - M;
@@ -286,7 +290,10 @@ __device__ __forceinline__ float3 fold_row_warp(const float4* rec, const ShardPl
                 ps += __shfl_xor_sync(0xFFFFFFFFu, ps, off);
                 pu += __shfl_xor_sync(0xFFFFFFFFu, pu, off);
             }
-            fold_shard(Ms, ps, pu, M, S, U);
+            const float dM = Ms - M;
+            const float f = expf(dM);
+            S = fmaf(ps, f, S);
+            U = fmaf(f, fmaf(dM, ps, pu), U);
         }
     }
     return make_float3(M, S, U);

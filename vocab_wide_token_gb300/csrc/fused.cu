@@ -160,7 +160,8 @@ __device__ __forceinline__ void unpack_vec<float>(const uint4& v, float (&x)[4])
 }
 
 // kBwd = false: pass 1 only (the forward: logprob, entropy, (M, ln S)).
-template <typename Ein, typename Eout, bool kBwd>
+// kShard (forward only): the per-shard statistics instead of the row outputs.
+template <typename Ein, typename Eout, bool kBwd, bool kShard = false>
 __global__ void __launch_bounds__(kFbWarps * 32, 1)
     fwdbwd_kernel(const Ein* __restrict__ logits, int64_t T, int64_t V, int64_t ld,
                   const __grid_constant__ ShardPlan plan, const int64_t* __restrict__ labels,
@@ -400,12 +401,12 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
                     const bool cached = tk.r < kFbRowCache;
                     const int64_t y = cached ? lab_s[tk.r] : (labels ? labels[t] : ignore_index);
                     const float w = cached ? wt_s[tk.r] : (weights ? weights[t] : 1.f);
-                    const int64_t yl = y - label_offset;  // the label's column here
+                    const int64_t yl = kShard ? y - label_offset : y;  // the label's column here
                     const bool y_in = y != ignore_index && yl >= 0 && yl < V;
                     float zy = 0.f;
                     if (lane == 0 && y_in) zy = Elem<Ein>::to_float(logits[t * ld + yl]);
                     const float3 st = fold_row_warp(records + b * kFbMaxChunks, plan, lane);
-                    if (lane == 0 && shard_out) {
+                    if (kShard && lane == 0) {
                         shard_out[t] = make_float4(st.x, st.y, st.z, zy);
                         mbar_arrive(&ready[b]);
                     } else if (lane == 0) {
@@ -528,7 +529,7 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
     }
 }
 
-template <typename Ein, typename Eout, bool kBwd>
+template <typename Ein, typename Eout, bool kBwd, bool kShard = false>
 cudaError_t launch_fused_t(const Ein* logits, int64_t T, int64_t V, int64_t ld,
                            const ShardPlan& plan, const int64_t* labels, int64_t ignore_index,
                            const float* weights, float* logprob, float* entropy, float* rowstats,
@@ -539,14 +540,14 @@ cudaError_t launch_fused_t(const Ein* logits, int64_t T, int64_t V, int64_t ld,
     int d = 0;
     cudaGetDevice(&d);
     if (d >= 64 || !configured[d].load(std::memory_order_acquire)) {
-        const cudaError_t e = cudaFuncSetAttribute(fwdbwd_kernel<Ein, Eout, kBwd>,
+        const cudaError_t e = cudaFuncSetAttribute(fwdbwd_kernel<Ein, Eout, kBwd, kShard>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    (int)kFusedSmem);
         if (e != cudaSuccess) return e;
         if (d < 64) configured[d].store(true, std::memory_order_release);
     }
     const int64_t grid = T < dev.sm_count ? T : dev.sm_count;
-    fwdbwd_kernel<Ein, Eout, kBwd><<<(unsigned)grid, kFbWarps * 32, kFusedSmem, stream>>>(
+    fwdbwd_kernel<Ein, Eout, kBwd, kShard><<<(unsigned)grid, kFbWarps * 32, kFusedSmem, stream>>>(
         logits, T, V, ld, plan, labels, ignore_index, weights, logprob, entropy, rowstats, out,
         ld_out, shard_out, label_offset, dev_error);
     return cudaGetLastError();
@@ -562,15 +563,23 @@ cudaError_t launch_forward_rows(const void* logits, pstat_dtype dt, int64_t T, i
                                 float* rowstats, int* dev_error, const DeviceInfo& dev,
                                 cudaStream_t stream, float4* shard_out, int64_t label_offset) {
     if (plan.n_chunks > kFbMaxChunks) return cudaErrorInvalidValue;
+    const uint16_t* zb = static_cast<const uint16_t*>(logits);
+    const float* zf = static_cast<const float*>(logits);
+    if (shard_out && dt == PSTAT_BF16)
+        return launch_fused_t<uint16_t, float, false, true>(
+            zb, T, V, ld, plan, labels, ignore_index, nullptr, logprob, entropy, rowstats, nullptr,
+            0, dev_error, dev, stream, shard_out, label_offset);
+    if (shard_out)
+        return launch_fused_t<float, float, false, true>(
+            zf, T, V, ld, plan, labels, ignore_index, nullptr, logprob, entropy, rowstats, nullptr,
+            0, dev_error, dev, stream, shard_out, label_offset);
     if (dt == PSTAT_BF16)
-        return launch_fused_t<uint16_t, float, false>(
-            static_cast<const uint16_t*>(logits), T, V, ld, plan, labels, ignore_index, nullptr,
-            logprob, entropy, rowstats, nullptr, 0, dev_error, dev, stream, shard_out,
-            label_offset);
-    return launch_fused_t<float, float, false>(static_cast<const float*>(logits), T, V, ld, plan,
-                                               labels, ignore_index, nullptr, logprob, entropy,
-                                               rowstats, nullptr, 0, dev_error, dev, stream,
-                                               shard_out, label_offset);
+        return launch_fused_t<uint16_t, float, false>(zb, T, V, ld, plan, labels, ignore_index,
+                                                      nullptr, logprob, entropy, rowstats, nullptr,
+                                                      0, dev_error, dev, stream);
+    return launch_fused_t<float, float, false>(zf, T, V, ld, plan, labels, ignore_index, nullptr,
+                                               logprob, entropy, rowstats, nullptr, 0, dev_error,
+                                               dev, stream);
 }
 
 }  // namespace pstat

@@ -189,11 +189,17 @@ int pstat_backward(const void* logits, pstat_dtype dt, int64_t T, int64_t V, int
         char* ws = static_cast<char*>(workspace);
         float4* cs = reinterpret_cast<float4*>(ws + wl.chunk_stats_off);
         float* rws = reinterpret_cast<float*>(ws + wl.rowstats_off);
-        if (launch_chunk_stats(logits, dt, T, ld, plan, cs, dev_error, dev, st) != cudaSuccess)
-            return PSTAT_ERR_CUDA;
-        if (launch_combine(cs, plan, logits, dt, T, V, ld, labels, ignore_index, nullptr, nullptr,
-                           nullptr, rws, dev_error, st) != cudaSuccess)
-            return PSTAT_ERR_CUDA;
+        if (plan.n_chunks <= forward_rows_max_chunks()) {
+            if (launch_forward_rows(logits, dt, T, V, ld, plan, labels, ignore_index, nullptr,
+                                    nullptr, rws, dev_error, dev, st) != cudaSuccess)
+                return PSTAT_ERR_CUDA;
+        } else {
+            if (launch_chunk_stats(logits, dt, T, ld, plan, cs, dev_error, dev, st) != cudaSuccess)
+                return PSTAT_ERR_CUDA;
+            if (launch_combine(cs, plan, logits, dt, T, V, ld, labels, ignore_index, nullptr,
+                               nullptr, nullptr, rws, dev_error, st) != cudaSuccess)
+                return PSTAT_ERR_CUDA;
+        }
         rs = rws;
     }
     if (launch_backward(logits, dt, T, V, ld, labels, ignore_index, weights, rs, out_dlogits,
