@@ -265,16 +265,20 @@ __device__ __forceinline__ void fold_shard(float Ms, float ps, float pu, float M
 
 __device__ __forceinline__ float3 fold_row_warp(const float4* rec, const ShardPlan& plan,
                                                 int lane) {
+    // With one shard its maximum is the row maximum: no separate pass.
     float M = -INFINITY;
-    for (int c = lane; c < plan.n_chunks; c += 32) M = fmaxf(M, rec[c].x);
-    M = warp_max(M);
+    if (plan.n_shards > 1) {
+        for (int c = lane; c < plan.n_chunks; c += 32) M = fmaxf(M, rec[c].x);
+        M = warp_max(M);
+    }
     float S = 0.f, U = 0.f;
-    if (M > -INFINITY) {
+    if (plan.n_shards == 1 || M > -INFINITY) {
         for (int sh = 0; sh < plan.n_shards; ++sh) {
             const int c0 = plan.cum[sh], c1 = plan.cum[sh + 1];
             float Ms = -INFINITY;
             for (int c = c0 + lane; c < c1; c += 32) Ms = fmaxf(Ms, rec[c].x);
             Ms = warp_max(Ms);
+            if (plan.n_shards == 1) M = Ms;
             if (Ms == -INFINITY) continue;
             float ps = 0.f, pu = 0.f;
             for (int c = c0 + lane; c < c1; c += 32) {
