@@ -210,16 +210,13 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
     }
     fence_mbar_init();
     __syncthreads();
-    // Pass 1 of row k: warp w owns chunks g = w, w + 13, ... .  Pass 2 shifts
-    // the assignment by n_chunks mod 13, so the warps that own one chunk more
-    // than the others in pass 1 are not all the ones that do in pass 2 (38
-    // chunks: warps 0..11 take 3 in pass 1, warp 12 takes 2; in pass 2 warp
-    // 11 takes 2).  With at least 13 chunks every warp owns chunks of every row in both
-    // passes, so it arrives for every row's fold and reads every row's
-    // statistics before the double-buffered records and row data are reused
-    // two rows later.  With fewer chunks there is no shift and warps without
-    // a chunk leave.
-    const int shift = nc >= kFbWarps ? nc % kFbWarps : 0;
+    // Both passes of row k: warp w owns chunks g = w, w + 13, ... .  Pass 2
+    // takes them starting with the last one, which is still in the warp's
+    // registers from pass 1 (no copy, no wait), then the others in order.
+    // With at least 13 chunks every warp owns chunks of every row, so it
+    // arrives for every row's fold and reads every row's statistics before the
+    // double-buffered records and row data are reused two rows later.  With
+    // fewer chunks warps without a chunk leave.
     if (nc < kFbWarps && warp >= nc) return;
 
     const uint64_t pol_keep = policy_evict_last();
@@ -237,7 +234,7 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
             c.cnt = 0;
             return;
         }
-        c.g0 = c.pass == 0 ? warp : (warp - shift + kFbWarps) % kFbWarps;
+        c.g0 = warp;
         c.cnt = c.g0 < nc ? (nc - c.g0 + kFbWarps - 1) / kFbWarps : 0;
     };
     auto settle = [&](Cursor& c) {  // first position at or after c that holds a chunk
@@ -258,6 +255,12 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
         settle(c);
     };
     auto done = [&](const Cursor& c) { return c.k >= nrows; };
+    // Pass 2's first position is the chunk pass 1 left in registers.
+    auto held = [&](const Cursor& c) { return kBwd && c.pass == 1 && c.i == 0; };
+    auto advance_issue = [&](Cursor& c) {  // next position that needs a copy
+        advance(c);
+        if (!done(c) && held(c)) advance(c);
+    };
 
     struct Task {
         int64_t r, t;  // the CTA's row index, token row
@@ -270,7 +273,8 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
     auto task_of = [&](const Cursor& c) {
         Task tk;
         tk.r = c.k;
-        tk.g = c.g0 + kFbWarps * c.i;
+        const int j = c.pass == 1 ? (c.i == 0 ? c.cnt - 1 : c.i - 1) : c.i;
+        tk.g = c.g0 + kFbWarps * j;
         tk.t = blockIdx.x + tk.r * gridDim.x;
         chunk_span(plan, tk.g, tk.start, tk.len);
         tk.src = logits + tk.t * ld + tk.start;
@@ -295,7 +299,7 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
     int64_t pi = 0;
     for (int s = 0; s < kFbStages && !done(ci); ++s, ++pi) {
         issue(ci, pi);
-        advance(ci);
+        advance_issue(ci);
     }
 
     Cursor cc = {0, 0, 0, 0, 0};  // position being consumed
@@ -304,8 +308,10 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
     uint32_t phase = 0;  // parity bit per ring slot
     bool failed = false;
     RowInfo ri = {{0.f, 0.f, 0.f, 0.f}, 0, 0.f, 0};
+    uint4 q[kVecPerLane];  // the chunk being processed; kept across positions for pass 2
     while (!done(cc)) {
         const Task tk = task_of(cc);
+        const bool hold = held(cc);  // data already in q
         const int b = (int)(tk.r & 1);
         const int slot = (int)(pc % kFbStages);
         Ein* buf = reinterpret_cast<Ein*>(slots + (size_t)slot * kSlotBytes);
@@ -334,31 +340,32 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
             ri = info[b];
         }
         const bool need_data = cc.pass == 0 || ri.mode == 2;
-        if (tk.bulk) {
-            bool ok = mbar_wait_bounded(&bars[slot], (phase >> slot) & 1u, kWaitLimitNs);
-            ok = __all_sync(0xFFFFFFFFu, ok);
-            if (!ok) {
-                failed = true;
-                break;
+        if (!hold) {
+            if (tk.bulk) {
+                bool ok = mbar_wait_bounded(&bars[slot], (phase >> slot) & 1u, kWaitLimitNs);
+                ok = __all_sync(0xFFFFFFFFu, ok);
+                if (!ok) {
+                    failed = true;
+                    break;
+                }
+                phase ^= 1u << slot;
+            } else if (need_data) {
+                // Unaligned chunk: element loads, padded with -inf to a whole vector.
+                const int padded = (len + kVec - 1) / kVec * kVec;
+                for (int k = lane; k < padded; k += 32)
+                    buf[k] = (k < len) ? tk.src[k] : Elem<Ein>::neg_inf();
+                __syncwarp();
             }
-            phase ^= 1u << slot;
-        } else if (need_data) {
-            // Unaligned chunk: element loads, padded with -inf to a whole vector.
-            const int padded = (len + kVec - 1) / kVec * kVec;
-            for (int k = lane; k < padded; k += 32)
-                buf[k] = (k < len) ? tk.src[k] : Elem<Ein>::neg_inf();
+            if (need_data) load_chunk_regs<Ein>(buf, len, lane, q);
             __syncwarp();
+            fence_proxy_async_smem();  // our reads of the slot precede the next bulk write into it
+            if (!done(ci)) {
+                issue(ci, pi);
+                advance_issue(ci);
+                ++pi;
+            }
         }
         const int nvec = (len + kVec - 1) / kVec;
-        uint4 q[kVecPerLane];
-        if (need_data) load_chunk_regs<Ein>(buf, len, lane, q);
-        __syncwarp();
-        fence_proxy_async_smem();  // our reads of the slot precede the next bulk write into it
-        if (!done(ci)) {
-            issue(ci, pi);
-            advance(ci);
-            ++pi;
-        }
 
         if (cc.pass == 0) {
             const float4 rec = reduce_regs(q, (Ein*)nullptr);
@@ -512,17 +519,21 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
                 }
             }
         }
+        if (!hold) ++pc;
         advance(cc);
-        ++pc;
     }
     if (failed) {
         if (lane == 0 && dev_error) atomicOr(dev_error, PSTAT_DEV_TIMEOUT);
-        // Drain copies still in flight into this CTA's shared memory before leaving.
-        for (int64_t p = pc; p < pi; ++p) {
-            if (task_of(cc).bulk) {
-                const int slot = (int)(p % kFbStages);
-                mbar_wait_bounded(&bars[slot], (phase >> slot) & 1u, kWaitLimitNs);
-                phase ^= 1u << slot;
+        // Drain copies still in flight into this CTA's shared memory before leaving
+        // (held positions had no copy).
+        for (int64_t p = pc; p < pi && !done(cc);) {
+            if (!held(cc)) {
+                if (task_of(cc).bulk) {
+                    const int slot = (int)(p % kFbStages);
+                    mbar_wait_bounded(&bars[slot], (phase >> slot) & 1u, kWaitLimitNs);
+                    phase ^= 1u << slot;
+                }
+                ++p;
             }
             advance(cc);
         }
