@@ -212,7 +212,10 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
     __syncthreads();
     // Both passes of row k: warp w owns chunks g = w, w + 13, ... .  Pass 2
     // takes them starting with the last one, which is still in the warp's
-    // registers from pass 1 (no copy, no wait), then the others in order.
+    // registers from pass 1, then the one before it, which is still in its
+    // bulk-copy slot (the refill that would have overwritten it is skipped:
+    // with two slots, pass 2's second copy position falls on exactly that
+    // slot), then the others in order, re-read from L2.
     // With at least 13 chunks every warp owns chunks of every row, so it
     // arrives for every row's fold and reads every row's statistics before the
     // double-buffered records and row data are reused two rows later.  With
@@ -255,9 +258,12 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
         settle(c);
     };
     auto done = [&](const Cursor& c) { return c.k >= nrows; };
-    // Pass 2's first position is the chunk pass 1 left in registers.
+    // Pass 2's first position is the chunk pass 1 left in registers (no slot);
+    // its second is the chunk pass 1 left in its slot (no copy).
+    static_assert(kFbStages == 2, "the slot-held chunk relies on a 2-slot ring");
     auto held = [&](const Cursor& c) { return kBwd && c.pass == 1 && c.i == 0; };
-    auto advance_issue = [&](Cursor& c) {  // next position that needs a copy
+    auto in_slot = [&](const Cursor& c) { return kBwd && c.pass == 1 && c.i == 1; };
+    auto advance_issue = [&](Cursor& c) {  // next position that uses a slot
         advance(c);
         if (!done(c) && held(c)) advance(c);
     };
@@ -273,7 +279,7 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
     auto task_of = [&](const Cursor& c) {
         Task tk;
         tk.r = c.k;
-        const int j = c.pass == 1 ? (c.i == 0 ? c.cnt - 1 : c.i - 1) : c.i;
+        const int j = c.pass == 0 ? c.i : c.i == 0 ? c.cnt - 1 : c.i == 1 ? c.cnt - 2 : c.i - 2;
         tk.g = c.g0 + kFbWarps * j;
         tk.t = blockIdx.x + tk.r * gridDim.x;
         chunk_span(plan, tk.g, tk.start, tk.len);
@@ -298,7 +304,7 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
     settle(ci);
     int64_t pi = 0;
     for (int s = 0; s < kFbStages && !done(ci); ++s, ++pi) {
-        issue(ci, pi);
+        if (!in_slot(ci)) issue(ci, pi);
         advance_issue(ci);
     }
 
@@ -311,7 +317,8 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
     uint4 q[kVecPerLane];  // the chunk being processed; kept across positions for pass 2
     while (!done(cc)) {
         const Task tk = task_of(cc);
-        const bool hold = held(cc);  // data already in q
+        const bool hold = held(cc);     // data already in q
+        const bool kept = in_slot(cc);  // data already in this slot
         const int b = (int)(tk.r & 1);
         const int slot = (int)(pc % kFbStages);
         Ein* buf = reinterpret_cast<Ein*>(slots + (size_t)slot * kSlotBytes);
@@ -341,7 +348,9 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
         }
         const bool need_data = cc.pass == 0 || ri.mode == 2;
         if (!hold) {
-            if (tk.bulk) {
+            if (kept) {
+                // left in the slot by pass 1; no copy was issued for it
+            } else if (tk.bulk) {
                 bool ok = mbar_wait_bounded(&bars[slot], (phase >> slot) & 1u, kWaitLimitNs);
                 ok = __all_sync(0xFFFFFFFFu, ok);
                 if (!ok) {
@@ -360,7 +369,7 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
             __syncwarp();
             fence_proxy_async_smem();  // our reads of the slot precede the next bulk write into it
             if (!done(ci)) {
-                issue(ci, pi);
+                if (!in_slot(ci)) issue(ci, pi);
                 advance_issue(ci);
                 ++pi;
             }
@@ -528,7 +537,7 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
         // (held positions had no copy).
         for (int64_t p = pc; p < pi && !done(cc);) {
             if (!held(cc)) {
-                if (task_of(cc).bulk) {
+                if (!in_slot(cc) && task_of(cc).bulk) {
                     const int slot = (int)(p % kFbStages);
                     mbar_wait_bounded(&bars[slot], (phase >> slot) & 1u, kWaitLimitNs);
                     phase ^= 1u << slot;
