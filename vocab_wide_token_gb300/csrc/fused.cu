@@ -428,42 +428,39 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
                     } else if (lane == 0) {
                         counter[b] = 0;
                         const float M = st.x, S = st.y, U = st.z;
-                        int err = 0;
-                        float lnS, H, lp;
+                        // First what pass 2 waits for -- ln S, the row's mode and
+                        // its gradient constants -- then publish; the entropy
+                        // (a division) and the global stores come after.
+                        const bool empty = !(M > -INFINITY);
+                        const bool bad = !empty && y != ignore_index && (y < 0 || y >= V);
+                        const float lnS = empty ? NAN : logf(S);
                         RowInfo nr;
-                        if (!(M > -INFINITY)) {
-                            err |= PSTAT_DEV_EMPTY_ROW;
-                            lnS = NAN;
+                        nr.mode = (y == ignore_index || w == 0.f) ? 0 : (empty || bad) ? 1 : 2;
+                        nr.gr = nr.mode == 2 ? grad_row(M, lnS, w) : GradRow{0.f, 0.f, 0.f, 0.f};
+                        nr.y = y;
+                        nr.zy = zy;
+                        info[b] = nr;
+                        mbar_arrive(&ready[b]);  // release: records, info visible to waiters
+                        float H, lp;
+                        if (empty) {
                             H = NAN;
                             lp = NAN;
                         } else {
-                            lnS = logf(S);
                             H = lnS - U / S;
                             if (y == ignore_index) {
                                 lp = 0.f;
-                            } else if (y < 0 || y >= V) {
-                                err |= PSTAT_DEV_BAD_LABEL;
+                            } else if (bad) {
                                 lp = NAN;
                                 H = NAN;
                             } else {
                                 lp = (zy - M) - lnS;
                             }
                         }
-                        if (y == ignore_index || w == 0.f)
-                            nr.mode = 0;
-                        else if (err)
-                            nr.mode = 1;
-                        else
-                            nr.mode = 2;
-                        nr.gr = nr.mode == 2 ? grad_row(M, lnS, w) : GradRow{0.f, 0.f, 0.f, 0.f};
-                        nr.y = y;
-                        nr.zy = zy;
-                        info[b] = nr;
                         if (logprob) logprob[t] = lp;
                         if (entropy) entropy[t] = H;
                         if (rowstats) reinterpret_cast<float2*>(rowstats)[t] = make_float2(M, lnS);
+                        const int err = (empty ? PSTAT_DEV_EMPTY_ROW : 0) | (bad ? PSTAT_DEV_BAD_LABEL : 0);
                         if (err && dev_error) atomicOr(dev_error, err);
-                        mbar_arrive(&ready[b]);  // release: records, info visible to waiters
                     }
                 }
                 __syncwarp();
