@@ -9,8 +9,10 @@
 //           as the chunk-statistics kernel does, into shared memory;
 //           the warp that finishes the row's last chunk folds the records in
 //           the fixed order of the combine kernel and publishes (M, ln S);
-//   pass 2  streams the same chunks again -- now from L2 -- and writes
-//           dlogits with the element-wise arithmetic of the backward kernel.
+//   pass 2  takes the same chunks again -- the warp's last one still in its
+//           registers, the one before still in its bulk-copy slot, the rest
+//           re-read from L2 -- and writes dlogits with the element-wise
+//           arithmetic of the backward kernel.
 // HBM sees 4V bytes per token (read once, write once).  Rows are dealt to
 // CTAs round robin; each warp keeps its 2-slot ring of bulk copies full
 // across both passes and across rows.  (Running pass 1 of the next row before
