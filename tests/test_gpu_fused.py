@@ -38,6 +38,7 @@ def _same_as_two_calls(pstat, z, y, w, bounds=None, out_dtype=None):
                                              (torch.float32, torch.bfloat16)])
 @pytest.mark.parametrize("V,bounds", [(10007, None), (10007, [0, 513, 6000, 10007]),
                                       (1001, None), (8, None), (7, None), (1, None),
+                                      (30000, None), (70000, None),
                                       (151936, [0, 50000, 100000, 151936])])
 def test_fused_bitwise_equals_two_calls(cuda_lib, dtype, out_dtype, V, bounds):
     g = torch.Generator(device="cuda").manual_seed(V + 17)
