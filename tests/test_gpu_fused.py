@@ -81,6 +81,36 @@ def test_fused_unaligned_rows_and_outputs(cuda_lib, offset):
     assert torch.equal(_bits(g1), _bits(g2))
 
 
+@pytest.mark.parametrize("dtype,V,offset,extra", [(torch.bfloat16, 1001, 0, 0),
+                                                (torch.bfloat16, 1001, 1, 0),
+                                                (torch.bfloat16, 4096, 1, 2),
+                                                (torch.bfloat16, 151936, 0, 1),
+                                                (torch.float32, 1001, 1, 0)])
+def test_label_logit_at_row_edges(cuda_lib, dtype, V, offset, extra):
+    """Labels on the first two and last two columns of rows whose starts fall
+    on either half of a 4-byte word (odd row strides and view offsets): the
+    label's logit is fetched as the aligned word that holds it, and where that
+    word would reach outside the row it is loaded on its own."""
+    T = 64
+    g = torch.Generator(device="cuda").manual_seed(V + offset + extra)
+    big = (2.0 * torch.randn(T, V + offset + extra, generator=g, device="cuda")).to(dtype)
+    z = big[:, offset:offset + V]
+    y = torch.empty(T, dtype=torch.int64, device="cuda")
+    y[0::4], y[1::4], y[2::4], y[3::4] = 0, V - 1, 1, V - 2
+    w = torch.randn(T, generator=g, device="cuda")
+    err = cuda_lib.new_error_flag(z.device)
+    lp, ent, rs = cuda_lib.forward(z, y, IGN, dev_error=err)
+    lp2, ent2, rs2, g2 = cuda_lib.forward_backward(z, y, w, IGN, dev_error=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert torch.equal(_bits(lp), _bits(lp2)) and torch.equal(_bits(ent), _bits(ent2))
+    zo, yo = to_oracle(z.contiguous()), y.cpu().numpy()
+    ref = oracle.forward(zo, yo, IGN)
+    assert_forward_close(lp2, ent2, ref, dtype, what=f"edge labels V={V}")
+    gref = oracle.backward(zo, yo, w.double().cpu().numpy(), IGN)
+    assert_grad_close(g2, gref, dtype, f"edge labels V={V}")
+
+
 def test_fused_device_errors(cuda_lib):
     T, V = 4, 3000
     z = torch.randn(T, V, device="cuda")
