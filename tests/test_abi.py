@@ -191,3 +191,43 @@ def test_shard_entry_argument_checks(lib):
     assert bwd(dt=1, out_dt=0) == -4
     assert bwd(start=50, total=120) == -2
     assert bwd(rs=0) == -1
+
+
+def test_binding_rejects_tensors_the_kernels_would_overrun(lib):
+    """The Python layer checks every tensor it hands to a kernel (dtype,
+    shape, device, layout) and raises before any launch.  The checks compare
+    devices only, so they run here against the CPU device."""
+    import torch
+
+    from vocab_wide_token_gb300 import pstat
+
+    cpu, T, V = torch.device("cpu"), 5, 7
+    f32 = torch.float32
+    # row outputs: right ones pass, a short or mistyped one does not
+    ok = (torch.empty(T), torch.empty(T), torch.empty(T, 2))
+    assert all(a is b for a, b in zip(pstat._row_outputs(ok, T, cpu), ok))
+    for bad in ((torch.empty(T - 1), ok[1], ok[2]), (ok[0], ok[1].double(), ok[2]),
+                (ok[0], ok[1], torch.empty(T, 3)), (ok[0], ok[1], torch.empty(2, T).t())):
+        with pytest.raises(ValueError):
+            pstat._row_outputs(bad, T, cpu)
+    # outputs on another device
+    with pytest.raises(ValueError):
+        pstat._row_outputs(ok, T, torch.device("cuda", 0))
+    # [T, V] outputs: rows may be padded, not overlap or be strided
+    big = torch.empty(T, V + 3, dtype=torch.bfloat16)
+    assert pstat._matrix_output(big[:, :V], T, V, cpu, "out") == V + 3
+    for bad in (torch.empty(T, V, dtype=torch.float16), torch.empty(V, T).t(),
+                torch.empty(T, V + 1)[:, 1:].as_strided((T, V), (V - 1, 1)),
+                torch.empty(T + 1, V)):
+        with pytest.raises(ValueError):
+            pstat._matrix_output(bad, T, V, cpu, "out")
+    with pytest.raises(ValueError):
+        pstat._weights(torch.empty(T, dtype=torch.float64), T, cpu)
+    with pytest.raises(ValueError):
+        pstat._rowstats(torch.empty(T, 2, dtype=f32).t().contiguous().t(), T, cpu)
+    with pytest.raises(ValueError):
+        pstat._error_flag(torch.zeros(1, dtype=torch.int64), cpu)
+    with pytest.raises(ValueError):
+        pstat._workspace(torch.empty(64, dtype=f32), 16, cpu)
+    assert pstat._workspace(None, 100, cpu).numel() == 100
+    assert pstat._rowstats(None, T, cpu) is None and pstat._weights(None, T, cpu) is None

@@ -211,3 +211,37 @@ def test_forward_past_256_chunks(cuda_lib):
     assert_forward_close(lp, ent, ref, torch.bfloat16, what="V > 256 chunks")
     with pytest.raises(cuda_lib.PstatError):
         cuda_lib.forward_backward(z, y, w, IGN)
+
+
+def test_bad_output_tensors_raise_before_launch(cuda_lib):
+    """Outputs on the host, of the wrong size or type, and inputs on the host
+    are rejected by the binding; nothing is launched and the device stays
+    usable."""
+    T, V = 16, 1000
+    z = torch.randn(T, V, device="cuda").to(torch.bfloat16)
+    y = torch.randint(0, V, (T,), device="cuda")
+    w = torch.randn(T, device="cuda")
+    lp, ent, rs = cuda_lib.forward(z, y, IGN)
+    host = (torch.empty(T), torch.empty(T), torch.empty(T, 2))
+    with pytest.raises(ValueError):
+        cuda_lib.forward(z, y, IGN, out=host)
+    with pytest.raises(ValueError):
+        cuda_lib.forward_backward(z, y, w, IGN, dlogits=torch.empty(T, V - 1, device="cuda",
+                                                                   dtype=torch.bfloat16))
+    with pytest.raises(ValueError):
+        cuda_lib.backward(z, y, w.cpu(), rs, IGN)
+    with pytest.raises(ValueError):
+        cuda_lib.backward(z, y, w, rs[:, :1], IGN)
+    with pytest.raises(ValueError):
+        cuda_lib.log_softmax(z, rs, out=torch.empty(T, V, device="cuda", dtype=torch.float16))
+    with pytest.raises(ValueError):
+        cuda_lib.forward(z, y, IGN, dev_error=torch.zeros(1, dtype=torch.int64, device="cuda"))
+    h = torch.randn(T, 64, device="cuda").to(torch.bfloat16)
+    W = torch.randn(V, 64, device="cuda").to(torch.bfloat16)
+    lph, enth, rsh = cuda_lib.lmhead_forward(h, W, y, IGN)
+    with pytest.raises(ValueError):
+        cuda_lib.lmhead_backward(h, W, y, w, rsh, IGN, dW=torch.zeros(V - 1, 64, device="cuda"))
+    # the device is still fine
+    lp2, ent2, rs2 = cuda_lib.forward(z, y, IGN)
+    torch.cuda.synchronize()
+    assert torch.equal(lp, lp2) and torch.equal(ent, ent2)

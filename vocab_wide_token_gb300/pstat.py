@@ -71,7 +71,7 @@ F32, BF16 = 0, 1
 OK = 0
 ERR = {-1: "NULLPTR", -2: "SHAPE", -3: "SHARDS", -4: "DTYPE", -5: "ALIGN", -6: "WORKSPACE",
        -7: "CUDA", -8: "UNSUPPORTED"}
-DEV_BAD_LABEL, DEV_EMPTY_ROW, DEV_TIMEOUT = 0x1, 0x2, 0x4
+DEV_BAD_LABEL, DEV_EMPTY_ROW, DEV_TIMEOUT, DEV_RANGE = 0x1, 0x2, 0x4, 0x8
 CHUNK_BF16, CHUNK_F32 = 4096, 2048
 MAX_SHARDS = 64
 
@@ -141,6 +141,70 @@ def _labels(labels, T, device):
     return labels.contiguous()
 
 
+# The kernels write through every pointer they get, so a tensor on another
+# device, of another size or with gaps would be written out of bounds: the
+# checks below reject it before anything is launched.
+def _tensor(x, dtype, shape, dev, name):
+    if (not isinstance(x, torch.Tensor) or x.dtype != dtype or tuple(x.shape) != tuple(shape)
+            or x.device != dev or not x.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)} "
+                         f"on {dev}")
+    return x
+
+
+def _row_outputs(out, T, dev):
+    """(logprob [T], entropy [T], rowstats [T, 2]), float32 on `dev`."""
+    if out is None:
+        return (torch.empty(T, dtype=torch.float32, device=dev),
+                torch.empty(T, dtype=torch.float32, device=dev),
+                torch.empty(T, 2, dtype=torch.float32, device=dev))
+    lp, ent, rs = out
+    return (_tensor(lp, torch.float32, (T,), dev, "out[0] (logprob)"),
+            _tensor(ent, torch.float32, (T,), dev, "out[1] (entropy)"),
+            _tensor(rs, torch.float32, (T, 2), dev, "out[2] (rowstats)"))
+
+
+def _matrix_output(out, T, V, dev, name):
+    """A [T, V] bf16 or fp32 output on `dev` with contiguous rows; returns its row stride."""
+    if (out.dim() != 2 or tuple(out.shape) != (T, V) or out.stride(1) != 1
+            or out.device != dev or out.dtype not in (torch.bfloat16, torch.float32)
+            or (T > 1 and out.stride(0) < V)):
+        raise ValueError(f"{name} must be a bf16 or fp32 [T, V] tensor on {dev} "
+                         "with contiguous rows")
+    return out.stride(0) if T > 1 else V
+
+
+def _weights(weights, T, dev):
+    if weights is None:
+        return None
+    if weights.dtype != torch.float32 or tuple(weights.shape) != (T,) or weights.device != dev:
+        raise ValueError(f"weights must be float32 [T] on {dev}")
+    return weights.contiguous()
+
+
+def _rowstats(rowstats, T, dev):
+    if rowstats is None:
+        return None
+    return _tensor(rowstats, torch.float32, (T, 2), dev, "rowstats")
+
+
+def _error_flag(flag, dev):
+    if flag is None:
+        return None
+    if (flag.dtype != torch.int32 or flag.numel() < 1 or flag.device != dev
+            or not flag.is_contiguous()):
+        raise ValueError(f"dev_error must be a contiguous int32 tensor on {dev}")
+    return flag
+
+
+def _workspace(ws, need, dev):
+    if ws is None:
+        return torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    if ws.dtype != torch.uint8 or ws.device != dev or not ws.is_contiguous():
+        raise ValueError(f"workspace must be a contiguous uint8 tensor on {dev}")
+    return ws
+
+
 def workspace_size(T: int, V: int, dtype: torch.dtype, shard_bounds=None) -> int:
     n = ctypes.c_size_t(0)
     arr, ns = _bounds(shard_bounds, V)
@@ -165,16 +229,11 @@ def forward(logits: torch.Tensor, labels: torch.Tensor | None, ignore_index: int
     T, V, ld = _rows(logits)
     dev = logits.device
     lab = _labels(labels, T, dev)
-    if out is None:
-        lp = torch.empty(T, dtype=torch.float32, device=dev)
-        ent = torch.empty(T, dtype=torch.float32, device=dev)
-        rs = torch.empty(T, 2, dtype=torch.float32, device=dev)
-    else:
-        lp, ent, rs = out
+    lp, ent, rs = _row_outputs(out, T, dev)
+    dev_error = _error_flag(dev_error, dev)
     arr, ns = _bounds(shard_bounds, V)
     need = workspace_size(T, V, logits.dtype, shard_bounds)
-    if workspace is None:
-        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    workspace = _workspace(workspace, need, dev)
     _check(_lib.pstat_forward(_ptr(logits), _dtype_code(logits), T, V, ld, _ptr(lab),
                               int(ignore_index), arr, ns, _ptr(lp), _ptr(ent), _ptr(rs),
                               _ptr(workspace), workspace.numel(), _ptr(dev_error), _stream(dev)),
@@ -195,12 +254,8 @@ def forward_noalloc(logits: torch.Tensor, labels: torch.Tensor | None, ignore_in
     T, V, ld = _rows(logits)
     dev = logits.device
     lab = _labels(labels, T, dev)
-    if out is None:
-        lp = torch.empty(T, dtype=torch.float32, device=dev)
-        ent = torch.empty(T, dtype=torch.float32, device=dev)
-        rs = torch.empty(T, 2, dtype=torch.float32, device=dev)
-    else:
-        lp, ent, rs = out
+    lp, ent, rs = _row_outputs(out, T, dev)
+    dev_error = _error_flag(dev_error, dev)
     arr, ns = _bounds(shard_bounds, V)
     _check(_lib.pstat_forward_noalloc(_ptr(logits), _dtype_code(logits), T, V, ld, _ptr(lab),
                                       int(ignore_index), arr, ns, _ptr(lp), _ptr(ent), _ptr(rs),
@@ -220,18 +275,15 @@ def backward(logits: torch.Tensor, labels: torch.Tensor | None, weights: torch.T
     out_dtype = out_dtype or logits.dtype
     if out is None:
         out = torch.empty(T, V, dtype=out_dtype, device=dev)
-    if out.dim() != 2 or out.shape != (T, V) or out.stride(1) != 1:
-        raise ValueError("out must be [T, V] with contiguous rows")
-    ld_out = out.stride(0) if T > 1 else V
-    w = None if weights is None else weights.contiguous()
-    if w is not None and (w.dtype != torch.float32 or w.shape != (T,)):
-        raise ValueError("weights must be float32 [T]")
+    ld_out = _matrix_output(out, T, V, dev, "out")
+    w = _weights(weights, T, dev)
+    rowstats = _rowstats(rowstats, T, dev)
+    dev_error = _error_flag(dev_error, dev)
     arr, ns = _bounds(shard_bounds, V)
     ws_ptr, ws_n = None, 0
     if rowstats is None:
         need = workspace_size(T, V, logits.dtype, shard_bounds)
-        if workspace is None:
-            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        workspace = _workspace(workspace, need, dev)
         ws_ptr, ws_n = _ptr(workspace), workspace.numel()
     _check(_lib.pstat_backward(_ptr(logits), _dtype_code(logits), T, V, ld, _ptr(lab),
                                int(ignore_index), _ptr(w), _ptr(rowstats), arr, ns, _ptr(out),
@@ -251,20 +303,12 @@ def forward_backward(logits: torch.Tensor, labels: torch.Tensor | None,
     dev = logits.device
     lab = _labels(labels, T, dev)
     out_dtype = out_dtype or logits.dtype
-    if out is None:
-        lp = torch.empty(T, dtype=torch.float32, device=dev)
-        ent = torch.empty(T, dtype=torch.float32, device=dev)
-        rs = torch.empty(T, 2, dtype=torch.float32, device=dev)
-    else:
-        lp, ent, rs = out
+    lp, ent, rs = _row_outputs(out, T, dev)
     if dlogits is None:
         dlogits = torch.empty(T, V, dtype=out_dtype, device=dev)
-    if dlogits.dim() != 2 or dlogits.shape != (T, V) or dlogits.stride(1) != 1:
-        raise ValueError("dlogits must be [T, V] with contiguous rows")
-    ld_out = dlogits.stride(0) if T > 1 else V
-    w = None if weights is None else weights.contiguous()
-    if w is not None and (w.dtype != torch.float32 or w.shape != (T,)):
-        raise ValueError("weights must be float32 [T]")
+    ld_out = _matrix_output(dlogits, T, V, dev, "dlogits")
+    w = _weights(weights, T, dev)
+    dev_error = _error_flag(dev_error, dev)
     arr, ns = _bounds(shard_bounds, V)
     _check(_lib.pstat_forward_backward(_ptr(logits), _dtype_code(logits), T, V, ld, _ptr(lab),
                                        int(ignore_index), _ptr(w), arr, ns, _ptr(lp), _ptr(ent),
@@ -288,8 +332,8 @@ def shard_stats(logits: torch.Tensor, labels: torch.Tensor | None, vocab_start: 
     lab = _labels(labels, T, dev)
     if out is None:
         out = torch.empty(T, 4, dtype=torch.float32, device=dev)
-    if out.shape != (T, 4) or not out.is_contiguous() or out.dtype != torch.float32:
-        raise ValueError("out must be a contiguous float32 [T, 4] tensor")
+    out = _tensor(out, torch.float32, (T, 4), dev, "out")
+    dev_error = _error_flag(dev_error, dev)
     _check(_lib.pstat_shard_stats(_ptr(logits), _dtype_code(logits), T, V, ld, _ptr(lab),
                                   int(ignore_index), int(vocab_start), _ptr(out),
                                   _ptr(dev_error), _stream(dev)), "pstat_shard_stats")
@@ -301,8 +345,9 @@ def combine_shards(stats: torch.Tensor, labels: torch.Tensor | None, shard_bound
     """Row outputs (logprob, entropy, rowstats) from gathered shard statistics
     stats [T, n_shards, 4], shards in ascending vocabulary order, bounds
     shard_bounds (n_shards + 1 ints from 0 to the vocabulary size)."""
-    if stats.dim() != 3 or stats.shape[2] != 4 or stats.dtype != torch.float32:
-        raise ValueError("stats must be float32 [T, n_shards, 4]")
+    if (stats.dim() != 3 or stats.shape[2] != 4 or stats.dtype != torch.float32
+            or not stats.is_cuda):
+        raise ValueError("stats must be a float32 CUDA tensor [T, n_shards, 4]")
     stats = stats.contiguous()
     T, ns = stats.shape[0], stats.shape[1]
     dev = stats.device
@@ -310,11 +355,8 @@ def combine_shards(stats: torch.Tensor, labels: torch.Tensor | None, shard_bound
     if nb != ns:
         raise ValueError("shard_bounds must have n_shards + 1 entries")
     lab = _labels(labels, T, dev)
-    if out is None:
-        out = (torch.empty(T, dtype=torch.float32, device=dev),
-               torch.empty(T, dtype=torch.float32, device=dev),
-               torch.empty(T, 2, dtype=torch.float32, device=dev))
-    lp, ent, rs = out
+    lp, ent, rs = _row_outputs(out, T, dev)
+    dev_error = _error_flag(dev_error, dev)
     _check(_lib.pstat_combine_shards(_ptr(stats), T, ns, arr, _ptr(lab), int(ignore_index),
                                      _ptr(lp), _ptr(ent), _ptr(rs), _ptr(dev_error),
                                      _stream(dev)), "pstat_combine_shards")
@@ -332,14 +374,14 @@ def backward_shard(logits: torch.Tensor, labels: torch.Tensor | None,
     out_dtype = out_dtype or logits.dtype
     if out is None:
         out = torch.empty(T, V, dtype=out_dtype, device=dev)
-    if out.dim() != 2 or out.shape != (T, V) or out.stride(1) != 1:
-        raise ValueError("out must be [T, V] with contiguous rows")
-    ld_out = out.stride(0) if T > 1 else V
-    w = None if weights is None else weights.contiguous()
-    if w is not None and (w.dtype != torch.float32 or w.shape != (T,)):
-        raise ValueError("weights must be float32 [T]")
+    ld_out = _matrix_output(out, T, V, dev, "out")
+    w = _weights(weights, T, dev)
+    if rowstats is None:
+        raise ValueError("rowstats (the global (M, ln S) per row) is required")
+    rowstats = _rowstats(rowstats, T, dev)
+    dev_error = _error_flag(dev_error, dev)
     _check(_lib.pstat_backward_shard(_ptr(logits), _dtype_code(logits), T, V, ld, _ptr(lab),
-                                     int(ignore_index), _ptr(w), _ptr(rowstats.contiguous()),
+                                     int(ignore_index), _ptr(w), _ptr(rowstats),
                                      int(vocab_start), int(vocab_total), _ptr(out),
                                      _dtype_code(out), ld_out, _ptr(dev_error), _stream(dev)),
            "pstat_backward_shard")
@@ -427,13 +469,14 @@ def log_softmax(logits: torch.Tensor, rowstats: torch.Tensor | None = None, shar
     out_dtype = out_dtype or logits.dtype
     if out is None:
         out = torch.empty(T, V, dtype=out_dtype, device=dev)
-    ld_out = out.stride(0) if T > 1 else V
+    ld_out = _matrix_output(out, T, V, dev, "out")
+    rowstats = _rowstats(rowstats, T, dev)
+    dev_error = _error_flag(dev_error, dev)
     arr, ns = _bounds(shard_bounds, V)
     ws_ptr, ws_n = None, 0
     if rowstats is None:
         need = workspace_size(T, V, logits.dtype, shard_bounds)
-        if workspace is None:
-            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        workspace = _workspace(workspace, need, dev)
         ws_ptr, ws_n = _ptr(workspace), workspace.numel()
     _check(_lib.pstat_log_softmax(_ptr(logits), _dtype_code(logits), T, V, ld, _ptr(rowstats), arr,
                                   ns, _ptr(out), _dtype_code(out), ld_out, ws_ptr, ws_n,
@@ -491,8 +534,10 @@ def lmhead_workspace_size(T: int, V: int, d: int) -> int:
 def _lmhead_args(hidden, W):
     if hidden.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
         raise TypeError("hidden and W must be bfloat16")
-    if not (hidden.is_cuda and W.is_cuda):
-        raise ValueError("hidden and W must be CUDA tensors")
+    if not (hidden.is_cuda and W.is_cuda) or hidden.device != W.device:
+        raise ValueError("hidden and W must be CUDA tensors on one device")
+    if hidden.dim() != 2 or W.dim() != 2:
+        raise ValueError("hidden must be [T, d] and W [V, d]")
     hidden, W = hidden.contiguous(), W.contiguous()
     T, d = hidden.shape
     V, d2 = W.shape
@@ -507,12 +552,9 @@ def lmhead_forward(hidden, W, labels, ignore_index: int = -100, *, workspace=Non
     hidden, W, T, V, d = _lmhead_args(hidden, W)
     dev = hidden.device
     lab = _labels(labels, T, dev)
-    lp = torch.empty(T, dtype=torch.float32, device=dev)
-    ent = torch.empty(T, dtype=torch.float32, device=dev)
-    rs = torch.empty(T, 2, dtype=torch.float32, device=dev)
-    if workspace is None:
-        workspace = torch.empty(max(lmhead_workspace_size(T, V, d), 16), dtype=torch.uint8,
-                                device=dev)
+    lp, ent, rs = _row_outputs(None, T, dev)
+    dev_error = _error_flag(dev_error, dev)
+    workspace = _workspace(workspace, lmhead_workspace_size(T, V, d), dev)
     _check(_lib.pstat_lmhead_fused(_ptr(hidden), _ptr(W), T, V, d, _ptr(lab), int(ignore_index),
                                    _ptr(lp), _ptr(ent), _ptr(rs), _ptr(workspace),
                                    workspace.numel(), _ptr(dev_error), _stream(dev)),
@@ -530,10 +572,14 @@ def lmhead_backward(hidden, W, labels, weights, rowstats, ignore_index: int = -1
         dhidden = torch.zeros(T, d, dtype=torch.float32, device=dev)
     if dW is None:
         dW = torch.zeros(V, d, dtype=torch.float32, device=dev)
-    w = None if weights is None else weights.contiguous()
-    if workspace is None:
-        workspace = torch.empty(max(lmhead_workspace_size(T, V, d), 16), dtype=torch.uint8,
-                                device=dev)
+    dhidden = _tensor(dhidden, torch.float32, (T, d), dev, "dhidden")
+    dW = _tensor(dW, torch.float32, (V, d), dev, "dW")
+    w = _weights(weights, T, dev)
+    if rowstats is None:
+        raise ValueError("rowstats (from lmhead_forward) is required")
+    rowstats = _rowstats(rowstats, T, dev)
+    dev_error = _error_flag(dev_error, dev)
+    workspace = _workspace(workspace, lmhead_workspace_size(T, V, d), dev)
     _check(_lib.pstat_lmhead_backward(_ptr(hidden), _ptr(W), T, V, d, _ptr(lab),
                                       int(ignore_index), _ptr(w), _ptr(rowstats), _ptr(dhidden),
                                       _ptr(dW), _ptr(workspace), workspace.numel(),
