@@ -59,12 +59,15 @@ constexpr size_t kInfoOff = kRecOff + 2 * kFbMaxChunks * sizeof(float4);
 constexpr size_t kReadyOff = kInfoOff + 2 * sizeof(RowInfo);
 constexpr size_t kRecsOff = kReadyOff + 2 * sizeof(uint64_t);  // forward only
 constexpr size_t kCountOff = kRecsOff + 2 * sizeof(uint64_t);
-// Labels and weights of the CTA's first kFbRowCache rows, loaded once at the
-// start so that the fold finds them in shared memory.
+// Labels, weights and label logits z_y of the CTA's first kFbRowCache rows,
+// loaded once at the start so that the fold finds them in shared memory (a
+// global load of z_y in the fold would put its latency on every row's
+// critical path).
 constexpr int kFbRowCache = 384;
 constexpr size_t kLabOff = (kCountOff + 2 * sizeof(int) + 7) / 8 * 8;
 constexpr size_t kWtOff = kLabOff + kFbRowCache * sizeof(int64_t);
-constexpr size_t kFusedSmem = kWtOff + kFbRowCache * sizeof(float);
+constexpr size_t kZyOff = kWtOff + kFbRowCache * sizeof(float);
+constexpr size_t kFusedSmem = kZyOff + kFbRowCache * sizeof(float);
 static_assert(kRingBytes % 16 == 0 && kRecOff % 16 == 0, "slots and records: 16-byte aligned");
 static_assert(kInfoOff % 8 == 0 && kReadyOff % 8 == 0, "RowInfo and mbarriers: 8-byte aligned");
 
@@ -189,6 +192,7 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
     int* counter = reinterpret_cast<int*>(smem + kCountOff);
     int64_t* lab_s = reinterpret_cast<int64_t*>(smem + kLabOff);
     float* wt_s = reinterpret_cast<float*>(smem + kWtOff);
+    float* zy_s = reinterpret_cast<float*>(smem + kZyOff);
 
     const int nc = plan.n_chunks;
     const int active = nc < kFbWarps ? nc : kFbWarps;  // warps that own chunks of any one row
@@ -207,8 +211,12 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
     const int64_t nrows = (T > (int64_t)blockIdx.x) ? (T - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     for (int64_t r = threadIdx.x; r < nrows && r < kFbRowCache; r += blockDim.x) {
         const int64_t t = blockIdx.x + r * gridDim.x;
-        lab_s[r] = labels ? labels[t] : ignore_index;
+        const int64_t y = labels ? labels[t] : ignore_index;
+        lab_s[r] = y;
         wt_s[r] = weights ? weights[t] : 1.f;
+        const int64_t yl = kShard ? y - label_offset : y;  // the label's column here
+        zy_s[r] = (y != ignore_index && yl >= 0 && yl < V) ? Elem<Ein>::to_float(logits[t * ld + yl])
+                                                           : 0.f;
     }
     fence_mbar_init();
     __syncthreads();
@@ -413,8 +421,8 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
                 }
                 if (fold_now) {
                     __threadfence_block();
-                    // Label, weight and z_y first: the z_y load then runs
-                    // under the fold's arithmetic.
+                    // Label, weight and z_y first (for rows past the cache
+                    // the z_y load then runs under the fold's arithmetic).
                     const int64_t t = tk.t;
                     const bool cached = tk.r < kFbRowCache;
                     const int64_t y = cached ? lab_s[tk.r] : (labels ? labels[t] : ignore_index);
@@ -422,7 +430,8 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
                     const int64_t yl = kShard ? y - label_offset : y;  // the label's column here
                     const bool y_in = y != ignore_index && yl >= 0 && yl < V;
                     float zy = 0.f;
-                    if (lane == 0 && y_in) zy = Elem<Ein>::to_float(logits[t * ld + yl]);
+                    if (lane == 0 && y_in)
+                        zy = cached ? zy_s[tk.r] : Elem<Ein>::to_float(logits[t * ld + yl]);
                     const float3 st = fold_row_warp(records + b * kFbMaxChunks, plan, lane);
                     if (kShard && lane == 0) {
                         shard_out[t] = make_float4(st.x, st.y, st.z, zy);
