@@ -30,8 +30,10 @@
  * the reduction the page describes for tensor-parallel shards: each shard
  * holds a local maximum, a local sum of exponentials and a local
  * entropy-weighted sum; a MAX reduction and SUM reductions combine them
- * (page 3 review thread answering why batch invariance survives, which
- * quotes the shard-local sum(exp(shifted)) followed by a SUM all-reduce).
+ * (torchtitan PR #4685, "[RL] Avoid full-vocab gather for TP policy
+ * statistics", the review thread on batch invariance: each shard sums the
+ * exponentials of its logits shifted by the global maximum, then a SUM
+ * all-reduce adds the shards).
  * It exists to check the invariant "shard-combined statistics equal the
  * full-vocabulary statistics".
  *
