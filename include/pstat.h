@@ -116,9 +116,9 @@ PSTAT_API int pstat_workspace_size(int64_t T, int64_t V, pstat_dtype dt, const i
 /*
  * Forward statistics: per-chunk statistics combined in a fixed order.  Plans
  * of at most 256 chunks per row run as one kernel with the records in shared
- * memory (the workspace is then not touched); larger plans run the
- * chunk-statistics kernel into the workspace, then the combine.  Both give
- * the same bits.
+ * memory (no workspace needed: it may be NULL and is not touched); larger
+ * plans run the chunk-statistics kernel into the workspace, then the combine.
+ * Both give the same bits.
  *   logits        [T, ld] dtype `dt`; element (t, v) at logits + t*ld + v.
  *                 Any alignment works; 16-byte aligned rows and chunk starts
  *                 take the bulk-copy path, others a slower path with the same
@@ -128,8 +128,9 @@ PSTAT_API int pstat_workspace_size(int64_t T, int64_t V, pstat_dtype dt, const i
  *                 n_shards <= PSTAT_MAX_SHARDS; NULL means {0, V}.
  *   out_logprob   [T] float (may be NULL), out_entropy [T] float (may be
  *                 NULL), out_rowstats [T, 2] float (M, ln S) (may be NULL).
- *   workspace     >= pstat_workspace_size(...) bytes, 16-byte aligned
- *                 (required either way).
+ *   workspace     >= pstat_workspace_size(...) bytes, 16-byte aligned;
+ *                 required only for plans of more than 256 chunks per row
+ *                 (PSTAT_ERR_WORKSPACE when it is missing there).
  *   dev_error     device int or NULL; bits PSTAT_DEV_*.
  * T = 0 is a no-op returning PSTAT_OK.
  */
@@ -140,6 +141,10 @@ PSTAT_API int pstat_forward(const void* logits, pstat_dtype dt, int64_t T, int64
 
 /* Bytes of the fixed device scratch used by pstat_forward_noalloc (8 MiB). */
 #define PSTAT_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* PSTAT_NOALLOC_SCRATCH_BYTES as built into this library, for bindings that
+ * cannot read the header. */
+PSTAT_API size_t pstat_noalloc_scratch_bytes(void);
 
 /*
  * pstat_forward for callers that cannot allocate device memory.  The pages
@@ -158,7 +163,9 @@ PSTAT_API int pstat_forward(const void* logits, pstat_dtype dt, int64_t T, int64
  *   else PSTAT_ERR_WORKSPACE is returned before anything is launched.
  *   The first call on each device looks up the scratch's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.
+ *   before any stream capture.  The address is cached per CUDA context
+ *   (cuCtxGetId): after cudaDeviceReset, the first call in the new context
+ *   looks it up again, so that call too belongs before any capture.
  *   Every call on a device shares the one scratch array, which keeps the last
  *   call's contents.  Nothing in it needs clearing (each call writes every
  *   record it reads), but calls whose kernels overlap on the GPU (different

@@ -12,8 +12,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "pstat.h")
 
 
-@pytest.fixture(scope="module")
-def lib():
+def _load():
     from vocab_wide_token_gb300 import build
 
     if not os.path.exists(build.LIB):
@@ -24,6 +23,26 @@ def lib():
     from vocab_wide_token_gb300 import pstat
 
     return pstat.lib()
+
+
+@pytest.fixture(scope="module")
+def exports():
+    """The library, for symbol and header checks (no calls that launch)."""
+    return _load()
+
+
+@pytest.fixture(scope="module")
+def lib():
+    """The library, for argument-check calls with made-up device addresses.
+    Every call below is meant to fail host-side validation; one that passed
+    it would reach device_info, which fails without a GPU.  With a GPU
+    present such a call would launch on those addresses, so these tests run
+    only where no CUDA device is visible."""
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("argument checks with made-up device pointers run only without a GPU")
+    return _load()
 
 
 def declared_symbols():
@@ -39,9 +58,9 @@ def test_header_declares_entry_points():
         assert must in names
 
 
-def test_exports_every_declared_symbol(lib):
+def test_exports_every_declared_symbol(exports):
     for name in declared_symbols():
-        assert hasattr(lib, name), f"libpstat.so does not export {name}"
+        assert hasattr(exports, name), f"libpstat.so does not export {name}"
 
 
 def test_status_strings(lib):
@@ -71,11 +90,14 @@ def test_forward_argument_checks(lib):
     assert _fwd(lib, bounds=list(range(0, 66)) + [100], ns=66) == -3  # too many shards
     assert _fwd(lib, T=0, logits=0) == 0               # empty batch is a no-op
     assert _fwd(lib, logits=0) == -1                   # null logits
-    assert _fwd(lib, ws=0) == -6                       # no workspace
-    assert _fwd(lib, ws_bytes=16) == -6                # workspace too small
     assert _fwd(lib, logits=0x1001) == -5              # bf16 logits must be 2-byte aligned
-    assert _fwd(lib, ws=0x2008) == -5                  # workspace must be 16-byte aligned
     assert _fwd(lib, labels=0x3004) == -5
+    # Up to 256 chunks per row the forward is one kernel and needs no
+    # workspace; past that the workspace is required, sized and aligned.
+    big = dict(V=4096 * 257, ld=4096 * 257)
+    assert _fwd(lib, ws=0, **big) == -6                # no workspace
+    assert _fwd(lib, ws_bytes=16, **big) == -6         # workspace too small
+    assert _fwd(lib, ws=0x2008, ws_bytes=1 << 30, **big) == -5  # 16-byte aligned workspace
 
 
 def test_workspace_size(lib):
@@ -231,3 +253,14 @@ def test_binding_rejects_tensors_the_kernels_would_overrun(lib):
         pstat._workspace(torch.empty(64, dtype=f32), 16, cpu)
     assert pstat._workspace(None, 100, cpu).numel() == 100
     assert pstat._rowstats(None, T, cpu) is None and pstat._weights(None, T, cpu) is None
+
+
+def test_noalloc_scratch_size_matches_header(exports):
+    # The binding sizes its checks from the library's exported value; both
+    # must agree with the header's PSTAT_NOALLOC_SCRATCH_BYTES.
+    from vocab_wide_token_gb300 import pstat
+
+    m = re.search(r"#define PSTAT_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", open(HEADER).read())
+    want = int(m.group(1)) << int(m.group(2))
+    exports.pstat_noalloc_scratch_bytes.restype = ctypes.c_size_t
+    assert exports.pstat_noalloc_scratch_bytes() == want == pstat.NOALLOC_SCRATCH_BYTES

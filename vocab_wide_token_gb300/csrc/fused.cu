@@ -564,16 +564,11 @@ cudaError_t launch_fused_t(const Ein* logits, int64_t T, int64_t V, int64_t ld,
                            Eout* out, int64_t ld_out, int* dev_error, const DeviceInfo& dev,
                            cudaStream_t stream, float4* shard_out = nullptr,
                            int64_t label_offset = 0) {
-    static std::atomic<bool> configured[64];
-    int d = 0;
-    cudaGetDevice(&d);
-    if (d >= 64 || !configured[d].load(std::memory_order_acquire)) {
-        const cudaError_t e = cudaFuncSetAttribute(fwdbwd_kernel<Ein, Eout, kBwd, kShard>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   (int)kFusedSmem);
-        if (e != cudaSuccess) return e;
-        if (d < 64) configured[d].store(true, std::memory_order_release);
-    }
+    static ContextSeen configured;
+    const cudaError_t e = ensure_smem_optin(
+        reinterpret_cast<const void*>(fwdbwd_kernel<Ein, Eout, kBwd, kShard>), (int)kFusedSmem,
+        configured);
+    if (e != cudaSuccess) return e;
     const int64_t grid = T < dev.sm_count ? T : dev.sm_count;
     fwdbwd_kernel<Ein, Eout, kBwd, kShard><<<(unsigned)grid, kFbWarps * 32, kFusedSmem, stream>>>(
         logits, T, V, ld, plan, labels, ignore_index, weights, logprob, entropy, rowstats, out,

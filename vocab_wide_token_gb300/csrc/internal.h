@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "pstat.h"
@@ -42,6 +43,27 @@ struct DeviceInfo {
     int max_smem_optin;
 };
 int device_info(DeviceInfo* info);  // PSTAT_OK / PSTAT_ERR_CUDA / PSTAT_ERR_UNSUPPORTED
+
+// Per-context set-up.  A kernel's shared-memory opt-in and the device address
+// of a __device__ array belong to the module loaded in one CUDA context; after
+// cudaDeviceReset the module is loaded again into a new context, where the
+// attribute is back at its default and the array may sit elsewhere.  Caches of
+// such set-up are therefore keyed on the context's process-unique id
+// (cuCtxGetId), never on the device index alone.
+constexpr int kMaxDevices = 64;
+
+// Id of the context current on this thread; 0 when none is current yet or
+// the driver cannot report it (callers then redo their set-up every time).
+uint64_t current_context_id();
+
+// For each device, the id of the context in which a one-time set-up last ran.
+struct ContextSeen {
+    std::atomic<uint64_t> id[kMaxDevices];
+};
+
+// cudaFuncSetAttribute(func, MaxDynamicSharedMemorySize, bytes), run once per
+// device and context.
+cudaError_t ensure_smem_optin(const void* func, int bytes, ContextSeen& seen);
 
 // Kernel launchers (stats_kernels.cu).  They assume validated arguments.
 cudaError_t launch_chunk_stats(const void* logits, pstat_dtype dt, int64_t T, int64_t ld,

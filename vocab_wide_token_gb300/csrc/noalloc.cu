@@ -16,7 +16,9 @@
 // the library's module is loaded on that GPU until the process exits).  Host
 // code cannot use the array's name as a device address, so the first call on
 // each device looks the address up with cudaGetSymbolAddress while that
-// device is current, and later calls reuse it.
+// device is current, and later calls reuse it.  The address belongs to the
+// context the module was loaded in: after cudaDeviceReset the next call finds
+// a new context (a new cuCtxGetId) and looks the address up again.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -32,24 +34,35 @@ static __device__ __align__(256) float4 g_noalloc_scratch[PSTAT_NOALLOC_SCRATCH_
 namespace pstat {
 namespace {
 
-constexpr int kMaxDevices = 64;
+struct ScratchAddress {
+    uint64_t ctx_id;  // context the address was looked up in (0: none yet)
+    float4* ptr;
+};
 std::mutex g_mu;
-float4* g_scratch_ptr[kMaxDevices] = {};
+ScratchAddress g_scratch[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (set-up on first
-// use).  Returns PSTAT_OK, PSTAT_ERR_CUDA or PSTAT_ERR_UNSUPPORTED.
-int scratch_for_current_device(float4** out) {
+// Device address of the scratch array in the current device's current
+// context, looked up on the first call in that context.  Returns PSTAT_OK,
+// PSTAT_ERR_CUDA or PSTAT_ERR_UNSUPPORTED.
+int scratch_for_current_context(float4** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PSTAT_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return PSTAT_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_mu);
-    if (g_scratch_ptr[dev] == nullptr) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
-            return PSTAT_ERR_CUDA;
-        g_scratch_ptr[dev] = static_cast<float4*>(p);
+    const uint64_t id = current_context_id();
+    if (id != 0 && g_scratch[dev].ctx_id == id) {
+        *out = g_scratch[dev].ptr;
+        return PSTAT_OK;
     }
-    *out = g_scratch_ptr[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+        return PSTAT_ERR_CUDA;
+    // The lookup has made the device's primary context current if it was not;
+    // with no context id to key on, nothing is cached and the next call looks
+    // the address up again.
+    g_scratch[dev].ctx_id = current_context_id();
+    g_scratch[dev].ptr = static_cast<float4*>(p);
+    *out = g_scratch[dev].ptr;
     return PSTAT_OK;
 }
 
@@ -57,6 +70,8 @@ int scratch_for_current_device(float4** out) {
 }  // namespace pstat
 
 using namespace pstat;
+
+extern "C" size_t pstat_noalloc_scratch_bytes(void) { return PSTAT_NOALLOC_SCRATCH_BYTES; }
 
 extern "C" int pstat_forward_noalloc(const void* logits, pstat_dtype dt, int64_t T, int64_t V,
                                      int64_t ld, const int64_t* labels, int64_t ignore_index,
@@ -84,7 +99,7 @@ extern "C" int pstat_forward_noalloc(const void* logits, pstat_dtype dt, int64_t
     rc = device_info(&dev);
     if (rc != PSTAT_OK) return rc;
     float4* cs = nullptr;
-    rc = scratch_for_current_device(&cs);
+    rc = scratch_for_current_context(&cs);
     if (rc != PSTAT_OK) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (launch_chunk_stats(logits, dt, T, ld, plan, cs, dev_error, dev, st) != cudaSuccess)

@@ -1,6 +1,7 @@
 // pstat_api.cu -- the extern "C" entry points of libpstat.so: argument
 // checks, workspace layout and kernel launches on the caller's stream.
 // Contracts are documented in include/pstat.h.
+#include <cuda.h>  // CUcontext, CUresult (types only; the driver is reached by entry point)
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -9,6 +10,52 @@
 #include "internal.h"
 
 namespace pstat {
+
+namespace {
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+void* driver_entry(const char* name) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return p;
+}
+}  // namespace
+
+uint64_t current_context_id() {
+    static std::once_flag once;
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    std::call_once(once, [] {
+        get_current = reinterpret_cast<CtxGetCurrentFn>(driver_entry("cuCtxGetCurrent"));
+        get_id = reinterpret_cast<CtxGetIdFn>(driver_entry("cuCtxGetId"));
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    unsigned long long id = 0;
+    if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return (uint64_t)id;
+}
+
+cudaError_t ensure_smem_optin(const void* func, int bytes, ContextSeen& seen) {
+    int d = 0;
+    const cudaError_t ge = cudaGetDevice(&d);
+    if (ge != cudaSuccess) return ge;
+    const bool slot = d >= 0 && d < kMaxDevices;
+    const uint64_t id = current_context_id();
+    if (slot && id != 0 && seen.id[d].load(std::memory_order_acquire) == id) return cudaSuccess;
+    const cudaError_t e =
+        cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    // The call above has made the device's primary context current if it was not.
+    const uint64_t now = current_context_id();
+    if (slot && now != 0) seen.id[d].store(now, std::memory_order_release);
+    return cudaSuccess;
+}
 
 int make_plan(int64_t V, int chunk, const int64_t* bounds, int n_shards, ShardPlan* plan) {
     if (bounds == nullptr) {
@@ -127,20 +174,24 @@ int pstat_forward(const void* logits, pstat_dtype dt, int64_t T, int64_t V, int6
     int rc = make_plan(V, chunk_for(dt), shard_bounds, n_shards, &plan);
     if (rc != PSTAT_OK) return rc;
     if (T == 0) return PSTAT_OK;
-    if (!logits || !workspace) return workspace ? PSTAT_ERR_NULLPTR : PSTAT_ERR_WORKSPACE;
+    if (!logits) return PSTAT_ERR_NULLPTR;
     if ((reinterpret_cast<uintptr_t>(logits) % elem_size(dt)) != 0) return PSTAT_ERR_ALIGN;
-    if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return PSTAT_ERR_ALIGN;
     if ((out_rowstats && (reinterpret_cast<uintptr_t>(out_rowstats) & 7u)) ||
         (labels && (reinterpret_cast<uintptr_t>(labels) & 7u)))
         return PSTAT_ERR_ALIGN;
+    // The one-kernel path keeps the chunk records in shared memory and needs
+    // no workspace; larger plans need one.
+    const bool one_kernel = plan.n_chunks <= forward_rows_max_chunks();
     const StatsWorkspace wl = stats_workspace_layout(T, plan);
-    if (ws_bytes < wl.total) return PSTAT_ERR_WORKSPACE;
+    if (!one_kernel) {
+        if (!workspace || ws_bytes < wl.total) return PSTAT_ERR_WORKSPACE;
+        if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return PSTAT_ERR_ALIGN;
+    }
     DeviceInfo dev;
     rc = device_info(&dev);
     if (rc != PSTAT_OK) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (plan.n_chunks <= forward_rows_max_chunks()) {
-        // one kernel; the workspace is not touched
+    if (one_kernel) {
         return launch_forward_rows(logits, dt, T, V, ld, plan, labels, ignore_index, out_logprob,
                                    out_entropy, out_rowstats, dev_error, dev, st) == cudaSuccess
                    ? PSTAT_OK

@@ -361,16 +361,11 @@ template <typename E>
 static cudaError_t launch_chunk_stats_t(const E* logits, int64_t T, int64_t ld,
                                         const ShardPlan& plan, float4* cs, int* dev_error,
                                         const DeviceInfo& dev, cudaStream_t stream) {
-    static std::atomic<bool> configured[64];
-    int d = 0;
-    cudaGetDevice(&d);
+    static ContextSeen configured;
     const size_t smem = chunk_stats_smem_bytes();
-    if (d >= 64 || !configured[d].load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(chunk_stats_kernel<E>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        if (d < 64) configured[d].store(true, std::memory_order_release);
-    }
+    const cudaError_t e = ensure_smem_optin(reinterpret_cast<const void*>(chunk_stats_kernel<E>),
+                                            (int)smem, configured);
+    if (e != cudaSuccess) return e;
     const int64_t items = T * plan.n_chunks;
     int64_t grid = (items + kWarps - 1) / kWarps;
     if (grid > dev.sm_count) grid = dev.sm_count;

@@ -66,6 +66,8 @@ _lib.pstat_combine_shards.restype = _i32
 _lib.pstat_backward_shard.argtypes = [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _i64,
                                       _i64, _vp, _i32, _i64, _vp, _vp]
 _lib.pstat_backward_shard.restype = _i32
+_lib.pstat_noalloc_scratch_bytes.argtypes = []
+_lib.pstat_noalloc_scratch_bytes.restype = _sz
 
 F32, BF16 = 0, 1
 OK = 0
@@ -86,6 +88,14 @@ class PstatError(RuntimeError):
 def _check(code: int, where: str) -> None:
     if code != OK:
         raise PstatError(code, where)
+
+
+def _call(dev, where: str, fn, *args) -> None:
+    """One ABI call with `dev` current: the library takes the device from
+    cudaGetDevice (device properties, per-context set-up, the no-allocation
+    scratch), so it must be the device that owns the tensors and the stream."""
+    with torch.cuda.device(dev):
+        _check(fn(*args), where)
 
 
 def lib() -> ctypes.CDLL:
@@ -213,6 +223,20 @@ def workspace_size(T: int, V: int, dtype: torch.dtype, shard_bounds=None) -> int
     return int(n.value)
 
 
+# pstat_forward runs as one kernel, with no workspace, up to this many chunks
+# per row (include/pstat.h).
+FORWARD_ROWS_MAX_CHUNKS = 256
+
+
+def n_chunks(V: int, dtype: torch.dtype, shard_bounds=None) -> int:
+    """Chunks per row of the plan: each shard is cut into whole chunks of
+    CHUNK_BF16 / CHUNK_F32 elements from its first column (shape arithmetic
+    for sizing only; the library validates the bounds)."""
+    c = CHUNK_BF16 if dtype == torch.bfloat16 else CHUNK_F32
+    b = [0, int(V)] if shard_bounds is None else [int(x) for x in shard_bounds]
+    return sum((b1 - b0 + c - 1) // c for b0, b1 in zip(b[:-1], b[1:]))
+
+
 def new_error_flag(device) -> torch.Tensor:
     """A device int for the kernels' error bits (PSTAT_DEV_*)."""
     return torch.zeros(1, dtype=torch.int32, device=device)
@@ -232,35 +256,37 @@ def forward(logits: torch.Tensor, labels: torch.Tensor | None, ignore_index: int
     lp, ent, rs = _row_outputs(out, T, dev)
     dev_error = _error_flag(dev_error, dev)
     arr, ns = _bounds(shard_bounds, V)
-    need = workspace_size(T, V, logits.dtype, shard_bounds)
-    workspace = _workspace(workspace, need, dev)
-    _check(_lib.pstat_forward(_ptr(logits), _dtype_code(logits), T, V, ld, _ptr(lab),
-                              int(ignore_index), arr, ns, _ptr(lp), _ptr(ent), _ptr(rs),
-                              _ptr(workspace), workspace.numel(), _ptr(dev_error), _stream(dev)),
-           "pstat_forward")
+    if workspace is None and n_chunks(V, logits.dtype, shard_bounds) > FORWARD_ROWS_MAX_CHUNKS:
+        workspace = _workspace(None, workspace_size(T, V, logits.dtype, shard_bounds), dev)
+    elif workspace is not None:
+        workspace = _workspace(workspace, 0, dev)
+    _call(dev, "pstat_forward", _lib.pstat_forward,
+          _ptr(logits), _dtype_code(logits), T, V, ld, _ptr(lab), int(ignore_index), arr, ns,
+          _ptr(lp), _ptr(ent), _ptr(rs), _ptr(workspace),
+          0 if workspace is None else workspace.numel(), _ptr(dev_error), _stream(dev))
     return lp, ent, rs
 
 
-NOALLOC_SCRATCH_BYTES = 8 << 20
+NOALLOC_SCRATCH_BYTES = int(_lib.pstat_noalloc_scratch_bytes())
 
 
 def forward_noalloc(logits: torch.Tensor, labels: torch.Tensor | None, ignore_index: int = -100,
                     shard_bounds=None, *, out=None, dev_error=None):
     """Like ``forward`` but through ``pstat_forward_noalloc``: no workspace is
     passed and the library allocates nothing; its scratch is a fixed
-    8 MiB array inside libpstat.so (T * n_chunks * 16 bytes must fit).  For
-    callers that may not allocate device memory at this point.  Calls that
-    overlap on the GPU share that scratch and race; keep them on one stream."""
+    NOALLOC_SCRATCH_BYTES array inside libpstat.so (T * n_chunks * 16 bytes
+    must fit).  For callers that may not allocate device memory at this
+    point.  Calls that overlap on the GPU share that scratch and race; keep
+    them on one stream."""
     T, V, ld = _rows(logits)
     dev = logits.device
     lab = _labels(labels, T, dev)
     lp, ent, rs = _row_outputs(out, T, dev)
     dev_error = _error_flag(dev_error, dev)
     arr, ns = _bounds(shard_bounds, V)
-    _check(_lib.pstat_forward_noalloc(_ptr(logits), _dtype_code(logits), T, V, ld, _ptr(lab),
-                                      int(ignore_index), arr, ns, _ptr(lp), _ptr(ent), _ptr(rs),
-                                      _ptr(dev_error), _stream(dev)),
-           "pstat_forward_noalloc")
+    _call(dev, "pstat_forward_noalloc", _lib.pstat_forward_noalloc,
+          _ptr(logits), _dtype_code(logits), T, V, ld, _ptr(lab), int(ignore_index), arr, ns,
+          _ptr(lp), _ptr(ent), _ptr(rs), _ptr(dev_error), _stream(dev))
     return lp, ent, rs
 
 
@@ -285,11 +311,10 @@ def backward(logits: torch.Tensor, labels: torch.Tensor | None, weights: torch.T
         need = workspace_size(T, V, logits.dtype, shard_bounds)
         workspace = _workspace(workspace, need, dev)
         ws_ptr, ws_n = _ptr(workspace), workspace.numel()
-    _check(_lib.pstat_backward(_ptr(logits), _dtype_code(logits), T, V, ld, _ptr(lab),
-                               int(ignore_index), _ptr(w), _ptr(rowstats), arr, ns, _ptr(out),
-                               _dtype_code(out), ld_out, ws_ptr, ws_n, _ptr(dev_error),
-                               _stream(dev)),
-           "pstat_backward")
+    _call(dev, "pstat_backward", _lib.pstat_backward,
+          _ptr(logits), _dtype_code(logits), T, V, ld, _ptr(lab), int(ignore_index), _ptr(w),
+          _ptr(rowstats), arr, ns, _ptr(out), _dtype_code(out), ld_out, ws_ptr, ws_n,
+          _ptr(dev_error), _stream(dev))
     return out
 
 
@@ -310,11 +335,10 @@ def forward_backward(logits: torch.Tensor, labels: torch.Tensor | None,
     w = _weights(weights, T, dev)
     dev_error = _error_flag(dev_error, dev)
     arr, ns = _bounds(shard_bounds, V)
-    _check(_lib.pstat_forward_backward(_ptr(logits), _dtype_code(logits), T, V, ld, _ptr(lab),
-                                       int(ignore_index), _ptr(w), arr, ns, _ptr(lp), _ptr(ent),
-                                       _ptr(rs), _ptr(dlogits), _dtype_code(dlogits), ld_out,
-                                       _ptr(dev_error), _stream(dev)),
-           "pstat_forward_backward")
+    _call(dev, "pstat_forward_backward", _lib.pstat_forward_backward,
+          _ptr(logits), _dtype_code(logits), T, V, ld, _ptr(lab), int(ignore_index), _ptr(w), arr,
+          ns, _ptr(lp), _ptr(ent), _ptr(rs), _ptr(dlogits), _dtype_code(dlogits), ld_out,
+          _ptr(dev_error), _stream(dev))
     return lp, ent, rs, dlogits
 
 
@@ -334,9 +358,9 @@ def shard_stats(logits: torch.Tensor, labels: torch.Tensor | None, vocab_start: 
         out = torch.empty(T, 4, dtype=torch.float32, device=dev)
     out = _tensor(out, torch.float32, (T, 4), dev, "out")
     dev_error = _error_flag(dev_error, dev)
-    _check(_lib.pstat_shard_stats(_ptr(logits), _dtype_code(logits), T, V, ld, _ptr(lab),
-                                  int(ignore_index), int(vocab_start), _ptr(out),
-                                  _ptr(dev_error), _stream(dev)), "pstat_shard_stats")
+    _call(dev, "pstat_shard_stats", _lib.pstat_shard_stats,
+          _ptr(logits), _dtype_code(logits), T, V, ld, _ptr(lab), int(ignore_index),
+          int(vocab_start), _ptr(out), _ptr(dev_error), _stream(dev))
     return out
 
 
@@ -357,9 +381,9 @@ def combine_shards(stats: torch.Tensor, labels: torch.Tensor | None, shard_bound
     lab = _labels(labels, T, dev)
     lp, ent, rs = _row_outputs(out, T, dev)
     dev_error = _error_flag(dev_error, dev)
-    _check(_lib.pstat_combine_shards(_ptr(stats), T, ns, arr, _ptr(lab), int(ignore_index),
-                                     _ptr(lp), _ptr(ent), _ptr(rs), _ptr(dev_error),
-                                     _stream(dev)), "pstat_combine_shards")
+    _call(dev, "pstat_combine_shards", _lib.pstat_combine_shards,
+          _ptr(stats), T, ns, arr, _ptr(lab), int(ignore_index), _ptr(lp), _ptr(ent), _ptr(rs),
+          _ptr(dev_error), _stream(dev))
     return lp, ent, rs
 
 
@@ -380,11 +404,10 @@ def backward_shard(logits: torch.Tensor, labels: torch.Tensor | None,
         raise ValueError("rowstats (the global (M, ln S) per row) is required")
     rowstats = _rowstats(rowstats, T, dev)
     dev_error = _error_flag(dev_error, dev)
-    _check(_lib.pstat_backward_shard(_ptr(logits), _dtype_code(logits), T, V, ld, _ptr(lab),
-                                     int(ignore_index), _ptr(w), _ptr(rowstats),
-                                     int(vocab_start), int(vocab_total), _ptr(out),
-                                     _dtype_code(out), ld_out, _ptr(dev_error), _stream(dev)),
-           "pstat_backward_shard")
+    _call(dev, "pstat_backward_shard", _lib.pstat_backward_shard,
+          _ptr(logits), _dtype_code(logits), T, V, ld, _ptr(lab), int(ignore_index), _ptr(w),
+          _ptr(rowstats), int(vocab_start), int(vocab_total), _ptr(out), _dtype_code(out), ld_out,
+          _ptr(dev_error), _stream(dev))
     return out
 
 
@@ -478,10 +501,9 @@ def log_softmax(logits: torch.Tensor, rowstats: torch.Tensor | None = None, shar
         need = workspace_size(T, V, logits.dtype, shard_bounds)
         workspace = _workspace(workspace, need, dev)
         ws_ptr, ws_n = _ptr(workspace), workspace.numel()
-    _check(_lib.pstat_log_softmax(_ptr(logits), _dtype_code(logits), T, V, ld, _ptr(rowstats), arr,
-                                  ns, _ptr(out), _dtype_code(out), ld_out, ws_ptr, ws_n,
-                                  _ptr(dev_error), _stream(dev)),
-           "pstat_log_softmax")
+    _call(dev, "pstat_log_softmax", _lib.pstat_log_softmax,
+          _ptr(logits), _dtype_code(logits), T, V, ld, _ptr(rowstats), arr, ns, _ptr(out),
+          _dtype_code(out), ld_out, ws_ptr, ws_n, _ptr(dev_error), _stream(dev))
     return out
 
 
@@ -500,9 +522,8 @@ def logprob_diff_metrics(logprob, rollout_logprob, labels=None, ignore_index: in
     b = _f32_vec(rollout_logprob, T, dev, "rollout_logprob")
     lab = _labels(labels, T, dev)
     out = torch.empty(4, dtype=torch.float32, device=dev)
-    _check(_lib.pstat_logprob_diff_metrics(_ptr(a), _ptr(b), _ptr(lab), int(ignore_index), T,
-                                           _ptr(out), _stream(dev)),
-           "pstat_logprob_diff_metrics")
+    _call(dev, "pstat_logprob_diff_metrics", _lib.pstat_logprob_diff_metrics,
+          _ptr(a), _ptr(b), _ptr(lab), int(ignore_index), T, _ptr(out), _stream(dev))
     return out
 
 
@@ -518,16 +539,16 @@ def clipped_surrogate(logprob, old_logprob, advantages, labels=None, eps_low: fl
     lab = _labels(labels, T, dev)
     loss = torch.empty(T, dtype=torch.float32, device=dev)
     weight = torch.empty(T, dtype=torch.float32, device=dev)
-    _check(_lib.pstat_clipped_surrogate(_ptr(a), _ptr(b), _ptr(c), _ptr(lab), int(ignore_index), T,
-                                        float(eps_low), float(eps_high), float(scale), _ptr(loss),
-                                        _ptr(weight), _stream(dev)),
-           "pstat_clipped_surrogate")
+    _call(dev, "pstat_clipped_surrogate", _lib.pstat_clipped_surrogate,
+          _ptr(a), _ptr(b), _ptr(c), _ptr(lab), int(ignore_index), T, float(eps_low),
+          float(eps_high), float(scale), _ptr(loss), _ptr(weight), _stream(dev))
     return loss, weight
 
 
 def lmhead_workspace_size(T: int, V: int, d: int) -> int:
     n = ctypes.c_size_t(0)
-    _check(_lib.pstat_lmhead_workspace_size(T, V, d, ctypes.byref(n)), "pstat_lmhead_workspace_size")
+    _check(_lib.pstat_lmhead_workspace_size(T, V, d, ctypes.byref(n)),
+           "pstat_lmhead_workspace_size")
     return int(n.value)
 
 
@@ -555,10 +576,9 @@ def lmhead_forward(hidden, W, labels, ignore_index: int = -100, *, workspace=Non
     lp, ent, rs = _row_outputs(None, T, dev)
     dev_error = _error_flag(dev_error, dev)
     workspace = _workspace(workspace, lmhead_workspace_size(T, V, d), dev)
-    _check(_lib.pstat_lmhead_fused(_ptr(hidden), _ptr(W), T, V, d, _ptr(lab), int(ignore_index),
-                                   _ptr(lp), _ptr(ent), _ptr(rs), _ptr(workspace),
-                                   workspace.numel(), _ptr(dev_error), _stream(dev)),
-           "pstat_lmhead_fused")
+    _call(dev, "pstat_lmhead_fused", _lib.pstat_lmhead_fused,
+          _ptr(hidden), _ptr(W), T, V, d, _ptr(lab), int(ignore_index), _ptr(lp), _ptr(ent),
+          _ptr(rs), _ptr(workspace), workspace.numel(), _ptr(dev_error), _stream(dev))
     return lp, ent, rs
 
 
@@ -580,11 +600,10 @@ def lmhead_backward(hidden, W, labels, weights, rowstats, ignore_index: int = -1
     rowstats = _rowstats(rowstats, T, dev)
     dev_error = _error_flag(dev_error, dev)
     workspace = _workspace(workspace, lmhead_workspace_size(T, V, d), dev)
-    _check(_lib.pstat_lmhead_backward(_ptr(hidden), _ptr(W), T, V, d, _ptr(lab),
-                                      int(ignore_index), _ptr(w), _ptr(rowstats), _ptr(dhidden),
-                                      _ptr(dW), _ptr(workspace), workspace.numel(),
-                                      _ptr(dev_error), _stream(dev)),
-           "pstat_lmhead_backward")
+    _call(dev, "pstat_lmhead_backward", _lib.pstat_lmhead_backward,
+          _ptr(hidden), _ptr(W), T, V, d, _ptr(lab), int(ignore_index), _ptr(w), _ptr(rowstats),
+          _ptr(dhidden), _ptr(dW), _ptr(workspace), workspace.numel(), _ptr(dev_error),
+          _stream(dev))
     return dhidden, dW
 
 
