@@ -76,3 +76,50 @@ def assert_grad_close(g, gref, out_dtype, what=""):
         idx = np.argwhere(~ok)[0]
         raise AssertionError(f"{what} dlogits{tuple(idx)}: gpu {a[tuple(idx)]!r} oracle "
                              f"{b[tuple(idx)]!r} ({int((~ok).sum())} bad elements)")
+
+
+class GradParity:
+    """The dlogits rule of ``assert_grad_close`` applied block by block on the
+    GPU, for full-size tensors: each block of oracle rows (float64, from the
+    CPU oracle) is moved to the device and compared element by element there;
+    the Frobenius-relative bound (bf16 outputs) is taken over all blocks."""
+
+    def __init__(self, out_dtype, what=""):
+        self.out_dtype = out_dtype
+        self.what = what
+        self.num = 0.0
+        self.den = 0.0
+        self.rows = 0
+
+    def add(self, g: torch.Tensor, gref: np.ndarray, row0: int = 0):
+        b = torch.from_numpy(np.ascontiguousarray(gref, np.float64)).to(g.device)
+        a = g.double()
+        nan_ok = torch.isnan(a) & torch.isnan(b)
+        if self.out_dtype == torch.float32:
+            ok = nan_ok | ((a - b).abs() <= 1e-3 * b.abs() + 1e-12)
+        else:
+            br = b.to(torch.bfloat16).double()
+            # one bf16 ulp at |b|: 2^(floor(log2|b|) - 7), floored at the
+            # subnormal spacing 2^-133.  frexp gives |b| = m 2^e, m in [0.5, 1);
+            # the power of two is assembled from its float64 bit pattern
+            # (exponent field k + 1023), exact on every device.
+            _, e = torch.frexp(b.abs().clamp_min(2.0**-126))
+            k = e.to(torch.int64) - 8
+            ulp = ((k + 1023) << 52).view(torch.float64).clamp_min(2.0**-133)
+            ok = nan_ok | ((a - br).abs() <= torch.maximum(1e-3 * b.abs(), ulp))
+            fin = torch.isfinite(b)
+            self.num += float(((a - b)[fin] ** 2).sum())
+            self.den += float((b[fin] ** 2).sum())
+        bad = ~ok
+        if bool(bad.any()):
+            idx = tuple(int(i) for i in torch.nonzero(bad)[0])
+            raise AssertionError(
+                f"{self.what} dlogits row {row0 + idx[0]} col {idx[1]}: gpu {float(a[idx])!r} "
+                f"oracle {float(b[idx])!r} ({int(bad.sum())} bad elements in this block)")
+        self.rows += g.shape[0]
+
+    def finish(self):
+        if self.out_dtype != torch.float32 and self.den > 0:
+            rel = (self.num / self.den) ** 0.5
+            assert rel <= 2.5e-3, f"{self.what} Frobenius-relative {rel}"
+        return self.rows

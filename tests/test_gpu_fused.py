@@ -63,6 +63,27 @@ def test_fused_bitwise_equals_two_calls(cuda_lib, dtype, out_dtype, V, bounds):
     assert_grad_close(gg, gref, out_dtype, f"fused V={V}")
 
 
+# A NaN payload no kernel produces: a store outside the T x V block of a
+# wider output buffer would overwrite it.
+CANARY16 = 0x7FA5
+CANARY32 = 0x7FC0A5A5
+
+
+def _canary_buffer(T, width, dtype):
+    if dtype == torch.bfloat16:
+        return torch.full((T, width), CANARY16, dtype=torch.int16, device="cuda").view(dtype)
+    return torch.full((T, width), CANARY32, dtype=torch.int32, device="cuda").view(dtype)
+
+
+def _assert_canary_intact(buf, c0, c1, what):
+    """Columns outside [c0, c1) of every row still hold the canary."""
+    bits = _bits(buf)
+    want = CANARY16 if buf.element_size() == 2 else CANARY32
+    outside = torch.cat([bits[:, :c0], bits[:, c1:]], dim=1)
+    bad = outside != want
+    assert not bool(bad.any()), f"{what}: {int(bad.sum())} elements outside the output overwritten"
+
+
 @pytest.mark.parametrize("offset", [1, 3])
 def test_fused_unaligned_rows_and_outputs(cuda_lib, offset):
     g = torch.Generator(device="cuda").manual_seed(offset)
@@ -73,12 +94,51 @@ def test_fused_unaligned_rows_and_outputs(cuda_lib, offset):
     w = torch.randn(T, generator=g, device="cuda")
     lp, ent, rs = cuda_lib.forward(z, y, IGN)
     g1 = cuda_lib.backward(z, y, w, rs, IGN)
-    outbig = torch.empty(T, V + 3, dtype=torch.bfloat16, device="cuda")
+    outbig = _canary_buffer(T, V + 3, torch.bfloat16)
     dl = outbig[:, 1:1 + V]
     lp2, ent2, rs2, g2 = cuda_lib.forward_backward(z, y, w, IGN, dlogits=dl)
     torch.cuda.synchronize()
     assert torch.equal(_bits(lp), _bits(lp2)) and torch.equal(_bits(ent), _bits(ent2))
     assert torch.equal(_bits(g1), _bits(g2))
+    _assert_canary_intact(outbig, 1, 1 + V, "forward_backward")
+
+
+@pytest.mark.parametrize("dtype,out_dtype,V,lead,tail",
+                         [(torch.bfloat16, torch.bfloat16, 9001, 1, 2),
+                          (torch.bfloat16, torch.bfloat16, 151936, 8, 8),
+                          (torch.float32, torch.float32, 10007, 3, 1),
+                          (torch.float32, torch.bfloat16, 4096, 1, 7)])
+def test_wider_outputs_keep_their_margins(cuda_lib, dtype, out_dtype, V, lead, tail):
+    """pstat_backward, pstat_forward_backward and pstat_log_softmax writing
+    into a view of a wider buffer (ld_out > V, first column at an offset)
+    touch nothing outside their T x V block, and give the same bits as with
+    a dense output."""
+    T = 37
+    g = torch.Generator(device="cuda").manual_seed(V + lead)
+    z = (2.0 * torch.randn(T, V, generator=g, device="cuda")).to(dtype)
+    y = torch.randint(0, V, (T,), generator=g, device="cuda")
+    y[2] = IGN
+    w = torch.randn(T, generator=g, device="cuda")
+    w[3] = 0.0
+    lp, ent, rs = cuda_lib.forward(z, y, IGN)
+    dense_b = cuda_lib.backward(z, y, w, rs, IGN, out_dtype=out_dtype)
+    dense_l = cuda_lib.log_softmax(z, rs, out_dtype=out_dtype)
+    width = lead + V + tail
+    for name in ("backward", "forward_backward", "log_softmax"):
+        buf = _canary_buffer(T, width, out_dtype)
+        view = buf[:, lead:lead + V]
+        if name == "backward":
+            cuda_lib.backward(z, y, w, rs, IGN, out_dtype=out_dtype, out=view)
+            dense = dense_b
+        elif name == "forward_backward":
+            cuda_lib.forward_backward(z, y, w, IGN, out_dtype=out_dtype, dlogits=view)
+            dense = dense_b
+        else:
+            cuda_lib.log_softmax(z, rs, out_dtype=out_dtype, out=view)
+            dense = dense_l
+        torch.cuda.synchronize()
+        _assert_canary_intact(buf, lead, lead + V, name)
+        assert torch.equal(_bits(view), _bits(dense)), name
 
 
 @pytest.mark.parametrize("dtype,V,offset,extra", [(torch.bfloat16, 1001, 0, 0),
