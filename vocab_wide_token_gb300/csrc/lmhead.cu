@@ -7,22 +7,36 @@
 // global memory.  The fixed-order combine kernel then gives logprob, entropy
 // and (M, ln S).
 //
-// Backward, per 8192-column vocabulary chunk c (the chunked lm_head of TRL PR
-// #6949 "ZeroSyncGRPOTrainer": GEMMs in a 16-bit dtype, accumulation in fp32
-// buffers):
+// Backward (the chunked lm_head of TRL PR #6949 "ZeroSyncGRPOTrainer": GEMMs
+// in a 16-bit dtype, accumulation in fp32 buffers).  With g = w q, where
+// q = onehot(y) - e^(z - M - ln S) lies in [-1, 1] and depends on the row
+// alone:
+//   0. once per call, W -> W16 = fp16(W) [V, d] and hidden -> h' =
+//      fp16(w_t hidden_t) [T, d] (one memory-bound launch);
+//   per 16384-column vocabulary chunk c:
 //   1. recompute the chunk's logits tile by tile and turn them on chip into
-//      g = w (onehot(y) - e^(z - M - ln S)), stored as fp16 twice: G [T, Vc]
-//      and its transpose Gt [Vc, T];
-//   2. dhidden += G W_c        (A = G, B = W_c^T, both K-major fp16);
-//   3. dW[c]   += Gt hidden    (A = Gt, B = hidden^T, both K-major fp16).
-// fp16 (11-bit significand) keeps the gradient operand within ~3e-4 relative
-// where bf16 would give ~2e-3; hidden and W convert to fp16 exactly while
-// 2^-14 <= |x| <= 65504 (values above flag PSTAT_DEV_RANGE).
+//      G = fp16(2^15 q) [T, Vc] (row-major);
+//   2. dhidden += (w_t 2^-15) (G W16_c)   A = G (K-major), B = W16_c read in
+//                                          place (MN-major);
+//   3. dW[c]   += 2^-15 (G^T h')          A = G read in place (MN-major),
+//                                          B = h' (MN-major).
+// Why the scale: at V = 151,936 nearly every softmax probability is below
+// 2^-14, where fp16 numbers are subnormal and lose relative precision; 2^15 q
+// keeps every |q| >= 2^-29 normal (and |2^15 q| <= 2^15 < 65504), so each
+// element carries one fp16 rounding (2^-12 relative) whatever its size.  The
+// weight is applied outside G (per output row of dhidden, folded into h' for
+// dW), so a token's G row -- and its dhidden row -- does not depend on the
+// other tokens of the batch.  fp16 (11-bit significand) rather than bf16
+// (8 bits, about 2e-3 relative) keeps dhidden and dW within 1e-3.  W converts
+// to fp16 exactly for 2^-14 <= |x| <= 65504; values above, and w hidden above
+// 65504, flag PSTAT_DEV_RANGE.
 //
 // One warp-specialised persistent GEMM kernel serves every step (192
 // threads, one CTA per SM):
 //   warp 0     TMA producer: 2-D tiled loads of A (128 x 64) and B (256 x 64)
-//              k-blocks into a 4-stage shared-memory ring (128-byte swizzle)
+//              k-blocks into a 4-stage shared-memory ring (128-byte swizzle);
+//              an operand stored with its M or N index contiguous (MN-major)
+//              arrives as 64 x 64 boxes and is read in place
 //   warp 1     allocates 512 TMEM columns (two 128 x 256 fp32 accumulators)
 //              and issues tcgen05.mma (M=128, N=256, K=16) from one thread
 //   warps 2-5  epilogue: one thread per output row reads its accumulator row
@@ -55,27 +69,53 @@ constexpr int BM = 128;            // output rows per tile (MMA M, TMEM lanes)
 constexpr int BN = 256;            // output columns per tile (MMA N)
 constexpr int BK = 64;             // K per stage: 64 x 16-bit = one 128-byte swizzle row
 constexpr int UK = 16;             // K per tcgen05.mma of kind::f16
-constexpr int STAGES = 4;
 // Statistics chunk of the fused forward: 2048 vocabulary columns (8 tiles),
 // folded in ascending tile order by one CTA.  Half the 4096 of the logits
 // path: at V = 151,936 a 16-tile unit leaves some SMs 32 units (512 tiles)
 // against an average of 500; 8-tile units cap that at 504.
 constexpr int LM_CHUNK = 2048;
 constexpr int STATS_TILES = LM_CHUNK / BN;
-constexpr int VC = 8192;           // backward vocabulary chunk (columns staged as G / Gt)
+// Backward vocabulary chunk (columns staged as G).  16384 columns give each
+// accumulation launch twice the units of 8192, halving the share of its last
+// partial wave: 38.1-38.6 against 39.2-39.4 ms per backward at T = 16384.
+constexpr int VC = 16384;
+// G holds 2^15 q, q = onehot(y) - p in [-1, 1]: no |q| >= 2^-29 is subnormal
+// in fp16 and |2^15 q| <= 32768 < 65504.
+constexpr float GRAD_SCALE = 32768.f;
+constexpr float GRAD_UNSCALE = 1.f / 32768.f;
 constexpr int M_GROUP = 32;        // M tiles sharing the L2-resident slice of A
-// The accumulation GEMMs (K = 8192 or T) stream a longer A slice per tile;
-// 16-tile groups measured about 1% faster there than 32 (8 and 64: slower).
-constexpr int ACC_M_GROUP = 16;
-constexpr int THREADS = 192;
-constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
+// The accumulation GEMMs run with 256-row tiles (TileCfg<true>): measured on
+// their shapes (8192 x 4096 x 16384 and 16384 x 4096 x 8192), 3% and 11%
+// faster than 128-row tiles, bit-identical.  Groups of 8 such tiles (2048
+// rows of A, as 16 tiles of 128 rows before) were within 1-2% of 4 and 16 and
+// ahead of 32.
+constexpr bool ACC_WIDE = true;
+constexpr int ACC_M_GROUP = 8;
 constexpr uint32_t B_BYTES = BN * BK * 2;   // 32 KB
-constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr uint32_t TMEM_COLS = 2 * BN;      // double-buffered accumulator
+constexpr uint32_t TMEM_COLS = 2 * BN;      // two 128 x 256 fp32 accumulators
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr int QD = 4;  // depth of the claimed-unit queue (dynamic scheduling)
 
-struct Smem {
+// Tile configuration of one GEMM kernel instantiation.
+//   kWide = false: 128 x 256 output tiles, 4 pipeline stages of 48 KB, the two
+//     TMEM accumulators double-buffer consecutive tiles, 4 epilogue warps.
+//   kWide = true: 256 x 256 output tiles computed as two M = 128 MMAs that
+//     share each B k-block, 3 stages of 64 KB, both accumulators hold one
+//     tile (no double buffer: the next tile waits for the drain), 8 epilogue
+//     warps (one per TMEM lane quadrant and accumulator).  Per k-block an SM
+//     loads 64 KB for 2 x 128 x 256 x 64 MMA work instead of 48 KB for half
+//     of it: a third less L2-to-SM operand traffic per flop, for GEMMs whose
+//     K is long enough to hide the undoubled drain.
+template <bool kWide>
+struct TileCfg {
+    static constexpr int TM = kWide ? 256 : 128;  // output rows per tile
+    static constexpr int HALVES = TM / BM;        // M = 128 MMAs per k-step
+    static constexpr int STAGES = kWide ? 3 : 4;
+    static constexpr uint32_t A_BYTES = TM * BK * 2;
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int EPI_WARPS = 4 * HALVES;
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    static constexpr int ACC_BUFS = kWide ? 1 : 2;  // tiles in flight in tensor memory
     // Offsets inside the 1024-byte aligned dynamic shared memory block.
     static constexpr uint32_t a = 0;
     static constexpr uint32_t b = a + STAGES * A_BYTES;
@@ -85,17 +125,44 @@ struct Smem {
     static constexpr uint32_t tmem_slot = bars + n_bars * 8;
     static constexpr uint32_t uq = tmem_slot + 16;  // int[QD]: claimed unit ids
     static constexpr uint32_t total = uq + QD * 4;
+    static constexpr size_t SMEM_BYTES = total + 1024;  // + alignment slack
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+    static_assert(a % 1024 == 0 && b % 1024 == 0 && A_BYTES % 1024 == 0,
+                  "stages must keep the 1 KB alignment of the 128-byte swizzle");
 };
-constexpr size_t SMEM_BYTES = Smem::total + 1024;  // + alignment slack
 
 struct GemmGeo {
     int m_tiles, n_tiles, k_blocks;
     int tiles_per_unit;   // consecutive N tiles one CTA processes in order
     int units_per_m;      // ceil(n_tiles / tiles_per_unit)
     int64_t n_units;      // m_tiles * units_per_m
-    int b_row0;           // first B row (tensor-map coordinate) of N tile 0
+    int b_n0;             // B's N coordinate of N tile 0 (tensor-map coordinate)
+    int b_k0;             // B's K coordinate of k-block 0
     int m_group;          // M tiles per group: units run M-fastest within a group
 };
+
+// Operand layouts, a compile-time parameter of the GEMM kernel (so the
+// K-major-only instantiations carry no layout code): bit 0 / 1 = problem 0's
+// A / B is MN-major, bit 2 / 3 = problem 1's.  K-major: a 2-D tensor map whose
+// inner coordinate is K; one box is [rows of M or N] x 64 K.  MN-major: a 4-D
+// tensor map {64 MN, 8 K rows, MN / 64, K / 8} (make_map_mn4d) and one box
+// {64, 8, tile / 64, 8} per stage, which lays the 1 KB swizzle atoms out
+// MN-first inside each 8-row K group: atom (K group g, MN block i) at
+// (g * tile / 64 + i) KB.  Measured on a 8192 x 4096 x 16384 fp16 GEMM, both
+// operands MN-major in this order run within 2% of both K-major, while one
+// 64 x 64 box per MN block (atoms 8 KB apart) ran 14% slower.
+__host__ __device__ constexpr uint32_t layout_bits(int a0, int b0, int a1, int b1) {
+    return (uint32_t)(a0 != 0) | ((uint32_t)(b0 != 0) << 1) | ((uint32_t)(a1 != 0) << 2) |
+           ((uint32_t)(b1 != 0) << 3);
+}
+template <uint32_t kLayout>
+__device__ __forceinline__ bool a_mn_of(int w) {
+    return ((kLayout >> (2 * w)) & 1u) != 0;
+}
+template <uint32_t kLayout>
+__device__ __forceinline__ bool b_mn_of(int w) {
+    return ((kLayout >> (2 * w + 1)) & 1u) != 0;
+}
 
 __host__ __device__ inline void unit_coords(const GemmGeo& g, int64_t u, int& m, int& un) {
     const int64_t per_group = (int64_t)g.m_group * g.units_per_m;
@@ -134,6 +201,11 @@ struct Problems {
 // Instruction descriptor for fp16 operands (A and B both f16, D fp32).
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
     return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// Operand-major bits of the instruction descriptor: bit 15 for A, bit 16 for
+// B; set = MN-major.
+__host__ __device__ constexpr uint32_t idesc_major(int a_mn, int b_mn) {
+    return ((uint32_t)(a_mn != 0) << 15) | ((uint32_t)(b_mn != 0) << 16);
 }
 
 // ---------------------------------------------------------------------------
@@ -251,10 +323,11 @@ struct StatsEpi {
     }
 };
 
-// Backward step 1: the recomputed logits tile becomes the gradient tile
-// g = w (onehot(y) - e^(z - M - ln S)), written as fp16 to G [rows, ldg]
-// (row-major) and Gt [cols, ldgt] (its transpose).  Rows past T, columns
-// past V, ignored rows and zero-weight rows are written as +0.
+// Backward step 1: the recomputed logits tile becomes the scaled gradient
+// tile 2^15 q = 2^15 (onehot(y) - e^(z - M - ln S)), written as fp16 to
+// G [rows, ldg] (row-major).  Rows past T, columns past V, ignored rows and
+// zero-weight rows are written as +0 (the weight itself is applied by the
+// accumulation GEMMs).
 struct GradEpi {
     int64_t T, V;
     int64_t c0;            // first vocabulary column of this chunk
@@ -264,14 +337,12 @@ struct GradEpi {
     const float2* rowstats;
     __half* G;
     int64_t ldg;
-    __half* Gt;
-    int64_t ldgt;
     int* dev_error;
 
     struct State {
         int64_t t, y;
         bool live;
-        float M, log2S, w;
+        float M, log2S;
     };
 
     __device__ void unit_begin(State& st, int m, int /*un*/, int row) const {
@@ -280,11 +351,10 @@ struct GradEpi {
         st.y = ignore_index;
         st.M = 0.f;
         st.log2S = 0.f;
-        st.w = 0.f;
         if (st.t < T) {
             st.y = labels ? labels[st.t] : ignore_index;
-            st.w = weights ? weights[st.t] : 1.f;
-            if (st.y != ignore_index && st.w != 0.f) {
+            const float w = weights ? weights[st.t] : 1.f;
+            if (st.y != ignore_index && w != 0.f) {
                 const float2 rs = rowstats[st.t];
                 st.M = rs.x;
                 st.log2S = rs.y * kLog2e;
@@ -304,8 +374,6 @@ struct GradEpi {
         const uint64_t negM = f2_pack(-st.M, -st.M);
         const uint64_t l2e = f2_pack(kLog2e, kLog2e);
         const uint64_t nl2s = f2_pack(-st.log2S, -st.log2S);
-        const float negw = -st.w;
-        bool range = false;
         for (int p = 0; p < BN / 32; ++p) {
             const int64_t jp = j0 + p * 32;
             float v[32];
@@ -318,22 +386,20 @@ struct GradEpi {
                     const uint64_t d = f2_add(f2_pack(v[i], v[i + 1]), negM);
                     float a0, a1;
                     f2_unpack(f2_fma(d, l2e, nl2s), a0, a1);
-                    g[i] = negw * ex2_approx(a0);
-                    g[i + 1] = negw * ex2_approx(a1);
+                    g[i] = -GRAD_SCALE * ex2_approx(a0);
+                    g[i + 1] = -GRAD_SCALE * ex2_approx(a1);
                 }
                 const int64_t yl = st.y - c0 - jp;
                 if (yl >= 0 && yl < 32) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        if (yl == i) g[i] = st.w + g[i];  // w (1 - p)
+                        if (yl == i) g[i] = GRAD_SCALE + g[i];  // 2^15 (1 - p)
                 }
                 const int64_t vcol = c0 + jp;  // vocabulary index of column i is vcol + i
                 if (vcol + 32 > V) {
                     for (int i = 0; i < 32; ++i)
                         if (vcol + i >= V) g[i] = 0.f;
                 }
-#pragma unroll
-                for (int i = 0; i < 32; ++i) range |= fabsf(g[i]) > 65504.f;
             } else {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) g[i] = 0.f;
@@ -349,25 +415,24 @@ struct GradEpi {
 #pragma unroll
             for (int i = 0; i < 4; ++i)
                 gp[i] = make_uint4(h2[4 * i], h2[4 * i + 1], h2[4 * i + 2], h2[4 * i + 3]);
-            // Gt column: the 32 lanes of the warp hold 32 consecutive tokens
-            __half* gtp = Gt + jp * ldgt + st.t;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) gtp[(int64_t)i * ldgt] = __float2half_rn(g[i]);
         }
-        if (range && dev_error) atomicOr(dev_error, PSTAT_DEV_RANGE);
     }
 
     __device__ void unit_end(State&, int, int, int) const {}
 };
 
-// Backward steps 2 and 3: out[row0 + r, c] += acc[r, c] for r < rows,
+// Backward steps 2 and 3: out[row0 + r, c] += f_r acc[r, c] for r < rows,
 // c < cols, with 16-byte vector reductions (each element has exactly one
-// writer per launch, so the result does not depend on timing).
+// writer per launch, so the result does not depend on timing).  The factor
+// is f_r = row_scale[r] * scale (row_scale may be NULL: f_r = scale); rows
+// with f_r == 0 are skipped.
 struct AccumEpi {
     float* out;
     int64_t ld;
     int64_t row0;
     int64_t rows, cols;
+    const float* row_scale;
+    float scale;
 
     struct State {};
 
@@ -376,16 +441,18 @@ struct AccumEpi {
     __device__ void tile(State&, uint32_t taddr, int m, int n, int row) const {
         const int64_t r = (int64_t)m * BM + row;
         const int64_t c0 = (int64_t)n * BN;
+        float f = 0.f;
+        if (r < rows) f = row_scale ? row_scale[r] * scale : scale;
         for (int p = 0; p < BN / 32; ++p) {
             float v[32];
             tmem_ld32(taddr + p * 32, v);
             tmem_ld_wait();
-            if (r >= rows) continue;
+            if (f == 0.f) continue;
             float* dst = out + (row0 + r) * ld + c0 + p * 32;
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
                 if (c0 + p * 32 + i + 4 <= cols)
-                    red_add_v4(dst + i, v[i], v[i + 1], v[i + 2], v[i + 3]);
+                    red_add_v4(dst + i, f * v[i], f * v[i + 1], f * v[i + 2], f * v[i + 3]);
             }
         }
     }
@@ -396,40 +463,42 @@ struct AccumEpi {
 // ---------------------------------------------------------------------------
 // The GEMM kernel.
 // ---------------------------------------------------------------------------
-template <class Epi, bool kF16>
-__global__ void __launch_bounds__(THREADS, 1)
+template <class Epi, bool kF16, uint32_t kLayout, bool kWide>
+__global__ void __launch_bounds__(TileCfg<kWide>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ Problems<Epi> P, int* __restrict__ dev_error) {
+    using C = TileCfg<kWide>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Smem::bars);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::bars);
     uint64_t* full = bars;
-    uint64_t* empty = bars + STAGES;
-    uint64_t* tfull = bars + 2 * STAGES;
+    uint64_t* empty = bars + C::STAGES;
+    uint64_t* tfull = bars + 2 * C::STAGES;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
     uint64_t* uq_full = drain + 1;
     uint64_t* uq_empty = uq_full + QD;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Smem::tmem_slot);
-    volatile int* uq = reinterpret_cast<volatile int*>(smem + Smem::uq);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::tmem_slot);
+    volatile int* uq = reinterpret_cast<volatile int*>(smem + C::uq);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const bool dynamic = P.counter != nullptr;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], 4);
+            mbar_init(&tempty[b], C::EPI_WARPS);
         }
         mbar_init(drain, 1);
         for (int q = 0; q < QD; ++q) {
-            mbar_init(&uq_full[q], 1);   // the producer publishes a unit
-            mbar_init(&uq_empty[q], 5);  // the MMA thread and the 4 epilogue warps took it
+            mbar_init(&uq_full[q], 1);  // the producer publishes a unit
+            // the MMA thread and every epilogue warp took it
+            mbar_init(&uq_empty[q], 1 + C::EPI_WARPS);
         }
         fence_mbar_init();
         prefetch_tensormap(&P.p[0].a);
@@ -494,32 +563,47 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int j = 0; j < nt && !failed; ++j) {
                     const int n = un * pr.g.tiles_per_unit + j;
                     for (int kb = 0; kb < pr.g.k_blocks; ++kb, ++it) {
-                        const int s = it % STAGES;
-                        const uint32_t ph = (it / STAGES) & 1u;
+                        const int s = it % C::STAGES;
+                        const uint32_t ph = (it / C::STAGES) & 1u;
                         if (!mbar_wait_bounded(&empty[s], ph ^ 1u, WAIT_NS)) {
                             failed = true;
                             break;
                         }
-                        mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-                        tma_load_2d(smem + Smem::a + s * A_BYTES, &pr.a, kb * BK, m * BM,
-                                    &full[s], pol_a);
-                        tma_load_2d(smem + Smem::b + s * B_BYTES, &pr.b, kb * BK,
-                                    pr.g.b_row0 + n * BN, &full[s], pol_b);
+                        mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+                        uint8_t* a_dst = smem + C::a + s * C::A_BYTES;
+                        uint8_t* b_dst = smem + C::b + s * B_BYTES;
+                        if (!a_mn_of<kLayout>(w))
+                            tma_load_2d(a_dst, &pr.a, kb * BK, m * C::TM, &full[s], pol_a);
+                        else
+                            tma_load_4d(a_dst, &pr.a, 0, 0, m * (C::TM / 64), kb * (BK / 8),
+                                        &full[s], pol_a);
+                        const int bk = pr.g.b_k0 + kb * BK;
+                        if (!b_mn_of<kLayout>(w))
+                            tma_load_2d(b_dst, &pr.b, bk, pr.g.b_n0 + n * BN, &full[s], pol_b);
+                        else
+                            tma_load_4d(b_dst, &pr.b, 0, 0, (pr.g.b_n0 + n * BN) / 64, bk / 8,
+                                        &full[s], pol_b);
                     }
                 }
             }
             // Every copy this thread issued must have landed before the CTA can
             // end (on the normal path they all have; after a timeout some may not).
-            for (uint32_t k = 0; k < (uint32_t)STAGES && k < it; ++k) {
+            for (uint32_t k = 0; k < (uint32_t)C::STAGES && k < it; ++k) {
                 const uint32_t i = it - 1 - k;
-                if (!mbar_wait_bounded(&full[i % STAGES], (i / STAGES) & 1u, WAIT_NS))
+                if (!mbar_wait_bounded(&full[i % C::STAGES], (i / C::STAGES) & 1u, WAIT_NS))
                     failed = true;
             }
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
-            constexpr uint32_t idesc = kF16 ? idesc_f16_f32(BM, BN) : idesc_bf16_f32(BM, BN);
+            constexpr uint32_t idesc0 = kF16 ? idesc_f16_f32(BM, BN) : idesc_bf16_f32(BM, BN);
+            // K-major: the K step moves 32 bytes along the swizzled row and the
+            // second 128-row half starts 128 rows x 128 bytes on.  MN-major
+            // (atoms MN-first): the next MN block is 1 KB on, the next 8-row K
+            // group (tile / 64) KB on, a K step of 16 rows spans two groups,
+            // and the second half starts two MN blocks on.
+            constexpr uint32_t a_kg = (C::TM / 64) * 1024, b_kg = (BN / 64) * 1024;
             uint32_t it = 0, tc = 0;
             for (int64_t i = 0; !failed; ++i) {
                 const int64_t u = consume_unit(i, true);
@@ -530,35 +614,46 @@ __global__ void __launch_bounds__(THREADS, 1)
                 int m, un;
                 unit_coords(g, u - (w ? P.n0 : 0), m, un);
                 const int nt = unit_tiles(g, un);
+                const bool a_mn = a_mn_of<kLayout>(w), b_mn = b_mn_of<kLayout>(w);
+                const uint32_t idesc = idesc0 | idesc_major(a_mn, b_mn);
                 for (int j = 0; j < nt && !failed; ++j, ++tc) {
-                    const uint32_t b = tc & 1u;
-                    const uint32_t tph = (tc >> 1) & 1u;
+                    const uint32_t b = tc % C::ACC_BUFS;
+                    const uint32_t tph = (tc / C::ACC_BUFS) & 1u;
                     if (!mbar_wait_bounded(&tempty[b], tph ^ 1u, WAIT_NS)) {
                         failed = true;
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t d_tmem = tmem_base + b * BN;
                     for (int kb = 0; kb < g.k_blocks; ++kb, ++it) {
-                        const int s = it % STAGES;
-                        const uint32_t ph = (it / STAGES) & 1u;
+                        const int s = it % C::STAGES;
+                        const uint32_t ph = (it / C::STAGES) & 1u;
                         if (!mbar_wait_bounded(&full[s], ph, WAIT_NS)) {
                             failed = true;
                             break;
                         }
                         tc_fence_after_sync();
-                        const uint32_t a_addr = smem_u32(smem + Smem::a + s * A_BYTES);
-                        const uint32_t b_addr = smem_u32(smem + Smem::b + s * B_BYTES);
+                        const uint32_t a_addr = smem_u32(smem + C::a + s * C::A_BYTES);
+                        const uint32_t b_addr = smem_u32(smem + C::b + s * B_BYTES);
 #pragma unroll
                         for (int kk = 0; kk < BK / UK; ++kk) {
-                            umma_bf16(d_tmem, sdesc_kmajor_sw128(a_addr + kk * UK * 2),
-                                      sdesc_kmajor_sw128(b_addr + kk * UK * 2), idesc,
-                                      (kb | kk) != 0);
+                            const uint64_t bd =
+                                b_mn ? sdesc_mnmajor_sw128(b_addr + kk * 2 * b_kg, 1024, b_kg)
+                                     : sdesc_kmajor_sw128(b_addr + kk * UK * 2);
+#pragma unroll
+                            for (int h = 0; h < C::HALVES; ++h) {
+                                const uint64_t ad =
+                                    a_mn ? sdesc_mnmajor_sw128(
+                                               a_addr + kk * 2 * a_kg + h * 2048, 1024, a_kg)
+                                         : sdesc_kmajor_sw128(a_addr + h * (BM * 128) +
+                                                              kk * UK * 2);
+                                const uint32_t d_tmem = tmem_base + (kWide ? h : b) * BN;
+                                umma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+                            }
                         }
                         umma_commit(&empty[s]);  // frees the stage once these MMAs finish
                     }
                     if (failed) break;
-                    umma_commit(&tfull[b]);      // accumulator b is ready
+                    umma_commit(&tfull[b]);      // the tile's accumulators are ready
                 }
             }
             // All MMAs issued by this thread complete before tensor memory is freed.
@@ -567,7 +662,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else {
         // ---------------- epilogue ----------------
-        const int q = warp & 3;  // TMEM lane quadrant of this warp
+        const int q = warp & 3;                   // TMEM lane quadrant of this warp
+        const int h = kWide ? (warp - 2) / 4 : 0;  // which 128-row half (wide tiles)
         const int row = q * 32 + lane;
         uint32_t tc = 0;
         typename Epi::State st;
@@ -583,11 +679,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             int m, un;
             unit_coords(pr.g, u - (w ? P.n0 : 0), m, un);
             const int nt = unit_tiles(pr.g, un);
-            pr.epi.unit_begin(st, m, un, row);
+            const int m128 = m * C::HALVES + h;  // this warp's 128-row tile
+            pr.epi.unit_begin(st, m128, un, row);
             for (int j = 0; j < nt; ++j, ++tc) {
                 const int n = un * pr.g.tiles_per_unit + j;
-                const uint32_t b = tc & 1u;
-                const uint32_t tph = (tc >> 1) & 1u;
+                const uint32_t b = tc % C::ACC_BUFS;
+                const uint32_t tph = (tc / C::ACC_BUFS) & 1u;
                 bool ok = mbar_wait_bounded(&tfull[b], tph, WAIT_NS);
                 ok = __all_sync(0xFFFFFFFFu, ok);
                 if (!ok) {
@@ -595,14 +692,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                pr.epi.tile(st, tmem_base + ((uint32_t)(q * 32) << 16) + b * BN, m, n, row);
-                // accumulator b may be overwritten from here on
+                pr.epi.tile(st, tmem_base + ((uint32_t)(q * 32) << 16) + (kWide ? h : b) * BN,
+                            m128, n, row);
+                // the accumulator may be overwritten once every epilogue warp arrived
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tempty[b]);
             }
             if (failed) break;
-            pr.epi.unit_end(st, m, un, row);
+            pr.epi.unit_end(st, m128, un, row);
         }
     }
 
@@ -616,32 +714,63 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Transpose with conversion to fp16: dst[c, r] = fp16(src[r, c]) for r < rows,
-// 0 for rows <= r < rows_pad; c < cols.  32 x 32 tiles through shared memory.
-// Values beyond the fp16 range set PSTAT_DEV_RANGE.
+// Backward step 0: W16 = fp16(W) [Vp, d] and h' = fp16(w_t hidden_t) [Tp, d]
+// (rows V <= v < Vp and T <= t < Tp as +0; weights NULL = 1), 8 elements per
+// thread and iteration, 16-byte loads and stores.  Values beyond the fp16
+// range set PSTAT_DEV_RANGE.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256)
-    transpose_bf16_to_f16(const uint16_t* __restrict__ src, int64_t rows, int64_t cols,
-                          int64_t ld_src, __half* __restrict__ dst, int64_t ld_dst,
-                          int64_t rows_pad, int* __restrict__ dev_error) {
-    __shared__ float tile[32][33];
-    const int64_t r0 = (int64_t)blockIdx.y * 32;
-    const int64_t c0 = (int64_t)blockIdx.x * 32;
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
-    bool range = false;
+__device__ __forceinline__ uint4 f16x8(const float (&x)[8], bool& range) {
+    uint32_t h[4];
 #pragma unroll
-    for (int k = 0; k < 32; k += 8) {
-        const int64_t r = r0 + ty + k, c = c0 + tx;
-        float x = 0.f;
-        if (r < rows && c < cols) x = __uint_as_float((uint32_t)src[r * ld_src + c] << 16);
-        range |= fabsf(x) > 65504.f;
-        tile[ty + k][tx] = x;
+    for (int i = 0; i < 4; ++i) {
+        range |= fabsf(x[2 * i]) > 65504.f || fabsf(x[2 * i + 1]) > 65504.f;
+        const __half2 v = __floats2half2_rn(x[2 * i], x[2 * i + 1]);
+        h[i] = *reinterpret_cast<const uint32_t*>(&v);
     }
-    __syncthreads();
+    return make_uint4(h[0], h[1], h[2], h[3]);
+}
+
+__global__ void __launch_bounds__(256)
+    to_fp16_kernel(const uint16_t* __restrict__ W, int64_t nW8, int64_t nWp8,
+                   __half* __restrict__ W16, const uint16_t* __restrict__ hidden,
+                   const float* __restrict__ weights, int64_t T, int64_t Tp, int64_t d8,
+                   __half* __restrict__ h16, int* __restrict__ dev_error) {
+    bool range = false;
+    const int64_t total = nWp8 + Tp * d8;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        float x[8];
+        uint4 out;
+        if (i >= nW8 && i < nWp8) {
+            reinterpret_cast<uint4*>(W16)[i] = make_uint4(0u, 0u, 0u, 0u);
+        } else if (i < nW8) {
+            const uint4 q = __ldcs(reinterpret_cast<const uint4*>(W) + i);
+            const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-    for (int k = 0; k < 32; k += 8) {
-        const int64_t c = c0 + ty + k, r = r0 + tx;
-        if (c < cols && r < rows_pad) dst[c * ld_dst + r] = __float2half_rn(tile[tx][ty + k]);
+            for (int k = 0; k < 4; ++k) {
+                x[2 * k] = bf2_lo(w4[k]);
+                x[2 * k + 1] = bf2_hi(w4[k]);
+            }
+            out = f16x8(x, range);
+            reinterpret_cast<uint4*>(W16)[i] = out;
+        } else {
+            const int64_t j = i - nWp8;
+            const int64_t t = j / d8;
+            if (t < T) {
+                const float wt = weights ? weights[t] : 1.f;
+                const uint4 q = __ldcs(reinterpret_cast<const uint4*>(hidden) + j);
+                const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    x[2 * k] = wt * bf2_lo(w4[k]);
+                    x[2 * k + 1] = wt * bf2_hi(w4[k]);
+                }
+                out = f16x8(x, range);
+            } else {
+                out = make_uint4(0u, 0u, 0u, 0u);
+            }
+            reinterpret_cast<uint4*>(h16)[j] = out;
+        }
     }
     if (range && dev_error) atomicOr(dev_error, PSTAT_DEV_RANGE);
 }
@@ -682,40 +811,57 @@ static bool make_map(CUtensorMap* map, bool f16, const void* ptr, int64_t rows, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-static GemmGeo geo(int64_t M, int64_t N, int64_t K, int tiles_per_unit, int64_t b_row0,
-                   int m_group = M_GROUP) {
+// M x N output, K-long reduction; B's N and K tensor-map coordinates start
+// at b_n0 and b_k0.
+// MN-major 16-bit matrix [K rows, MN cols] (row stride ld elements; MN a
+// multiple of 64, K a multiple of 8) -> 4-D tensor map {64, 8, MN / 64, K / 8}
+// whose box {64, 8, tile_mn / 64, BK / 8} lays the swizzle atoms out MN-first
+// within each 8-row K group.
+static bool make_map_mn4d(CUtensorMap* map, const void* ptr, int64_t krows, int64_t mn,
+                          int64_t ld, int tile_mn) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || mn % 64 != 0 || krows % 8 != 0) return false;
+    const cuuint64_t dims[4] = {64, 8, (cuuint64_t)(mn / 64), (cuuint64_t)(krows / 8)};
+    const cuuint64_t strides[3] = {(cuuint64_t)ld * 2, 128, (cuuint64_t)ld * 2 * 8};
+    const cuuint32_t box[4] = {64, 8, (cuuint32_t)(tile_mn / 64), (cuuint32_t)(BK / 8)};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static GemmGeo geo(int64_t M, int64_t N, int64_t K, int tiles_per_unit, int64_t b_n0,
+                   int m_group = M_GROUP, int64_t b_k0 = 0, int tile_m = BM) {
     GemmGeo g;
     g.m_group = m_group;
-    g.m_tiles = (int)((M + BM - 1) / BM);
+    g.m_tiles = (int)((M + tile_m - 1) / tile_m);
     g.n_tiles = (int)((N + BN - 1) / BN);
     g.k_blocks = (int)((K + BK - 1) / BK);
     g.tiles_per_unit = tiles_per_unit;
     g.units_per_m = (g.n_tiles + tiles_per_unit - 1) / tiles_per_unit;
     g.n_units = (int64_t)g.m_tiles * g.units_per_m;
-    g.b_row0 = (int)b_row0;
+    g.b_n0 = (int)b_n0;
+    g.b_k0 = (int)b_k0;
     return g;
 }
 
-template <class Epi, bool kF16>
+template <class Epi, bool kF16, uint32_t kLayout, bool kWide>
 static cudaError_t launch_problems(const Problems<Epi>& P, int* dev_error, int sm_count,
                                    cudaStream_t st) {
-    static std::atomic<bool> configured[64];
-    int devi = 0;
-    cudaGetDevice(&devi);
-    if (devi >= 64 || !configured[devi].load()) {
-        const cudaError_t e =
-            cudaFuncSetAttribute(tc_gemm_kernel<Epi, kF16>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        if (devi < 64) configured[devi].store(true);
-    }
+    using C = TileCfg<kWide>;
+    static ContextSeen configured;
+    const cudaError_t e = ensure_smem_optin(
+        reinterpret_cast<const void*>(tc_gemm_kernel<Epi, kF16, kLayout, kWide>),
+        (int)C::SMEM_BYTES, configured);
+    if (e != cudaSuccess) return e;
     if (P.total == 0) return cudaSuccess;
     const int64_t grid = P.total < sm_count ? P.total : sm_count;
-    tc_gemm_kernel<Epi, kF16><<<(unsigned)grid, THREADS, SMEM_BYTES, st>>>(P, dev_error);
+    tc_gemm_kernel<Epi, kF16, kLayout, kWide>
+        <<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, st>>>(P, dev_error);
     return cudaGetLastError();
 }
 
-// One GEMM, static round-robin schedule.
+// One GEMM, static round-robin schedule, both operands K-major.
 template <class Epi, bool kF16>
 static cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmGeo& g,
                                const Epi& epi, int* dev_error, int sm_count, cudaStream_t st) {
@@ -728,12 +874,14 @@ static cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, con
     P.n0 = g.n_units;
     P.total = g.n_units;
     P.counter = nullptr;
-    return launch_problems<Epi, kF16>(P, dev_error, sm_count, st);
+    return launch_problems<Epi, kF16, 0u, false>(P, dev_error, sm_count, st);
 }
 
-// Two GEMMs in one launch, units claimed through `counter` (zeroed before).
-// The first problem should be the one with the longer units.
-template <class Epi, bool kF16>
+// Two GEMMs in one launch, units claimed through `counter` (zeroed before),
+// operand layouts kLayout, tile configuration kWide (the geometries' M tiles
+// must be TileCfg<kWide>::TM rows).  The first problem should be the one with
+// the longer units.
+template <class Epi, bool kF16, uint32_t kLayout, bool kWide>
 static cudaError_t launch_gemm_pair(const CUtensorMap& ma0, const CUtensorMap& mb0,
                                     const GemmGeo& g0, const Epi& e0, const CUtensorMap& ma1,
                                     const CUtensorMap& mb1, const GemmGeo& g1, const Epi& e1,
@@ -750,49 +898,22 @@ static cudaError_t launch_gemm_pair(const CUtensorMap& ma0, const CUtensorMap& m
     P.n0 = g0.n_units;
     P.total = g0.n_units + g1.n_units;
     P.counter = counter;
-    return launch_problems<Epi, kF16>(P, dev_error, sm_count, st);
+    return launch_problems<Epi, kF16, kLayout, kWide>(P, dev_error, sm_count, st);
 }
 
-static cudaError_t launch_transpose(const uint16_t* src, int64_t rows, int64_t cols,
-                                    int64_t ld_src, __half* dst, int64_t ld_dst, int64_t rows_pad,
-                                    int* dev_error, cudaStream_t st) {
-    const dim3 grid((unsigned)((cols + 31) / 32), (unsigned)((rows_pad + 31) / 32));
-    transpose_bf16_to_f16<<<grid, 256, 0, st>>>(src, rows, cols, ld_src, dst, ld_dst, rows_pad,
-                                                 dev_error);
+static cudaError_t launch_to_fp16(const void* W, int64_t V, int64_t Vp, const void* hidden,
+                                  const float* weights, int64_t T, int64_t Tp, int64_t d,
+                                  __half* W16, __half* h16, int* dev_error, int sm_count,
+                                  cudaStream_t st) {
+    const int64_t nW8 = V * d / 8, nWp8 = Vp * d / 8, d8 = d / 8;
+    const int64_t total = nWp8 + Tp * d8;
+    int64_t grid = (total + 255) / 256;
+    if (grid > (int64_t)sm_count * 8) grid = (int64_t)sm_count * 8;
+    to_fp16_kernel<<<(unsigned)grid, 256, 0, st>>>(
+        static_cast<const uint16_t*>(W), nW8, nWp8, W16, static_cast<const uint16_t*>(hidden),
+        weights, T, Tp, d8, h16, dev_error);
     return cudaGetLastError();
 }
-
-// A stream and events of one backward call: the W transposes run there, next
-// to the GEMMs on the caller's stream.  Created per call and released at the
-// end of it (destruction waits for nothing; the driver frees them once their
-// work is done), so concurrent calls never share them.  Once forked from the
-// caller's stream, the side stream is joined back into it when this object
-// goes out of scope -- on every return path, errors included -- so nothing
-// the call queued can outlive the caller's view of it.
-struct SideStream {
-    cudaStream_t s = nullptr, caller = nullptr;
-    cudaEvent_t start = nullptr, hT = nullptr, done = nullptr, tr[2] = {}, acc[2] = {};
-    bool ok = false, forked = false;
-    SideStream() {
-        ok = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) == cudaSuccess;
-        for (cudaEvent_t* e : {&start, &hT, &done, &tr[0], &tr[1], &acc[0], &acc[1]})
-            ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
-    }
-    // The side stream's work starts after everything queued so far on `c`.
-    bool fork(cudaStream_t c) {
-        caller = c;
-        forked = cudaEventRecord(start, c) == cudaSuccess &&
-                 cudaStreamWaitEvent(s, start, 0) == cudaSuccess;
-        return forked;
-    }
-    ~SideStream() {
-        if (forked && cudaEventRecord(done, s) == cudaSuccess)
-            cudaStreamWaitEvent(caller, done, 0);
-        for (cudaEvent_t e : {start, hT, done, tr[0], tr[1], acc[0], acc[1]})
-            if (e) cudaEventDestroy(e);
-        if (s) cudaStreamDestroy(s);
-    }
-};
 
 // ---- workspace layouts -------------------------------------------------------------
 struct FwdWorkspace {
@@ -809,18 +930,18 @@ static FwdWorkspace fwd_layout(int64_t T, int64_t V) {
 
 struct BwdWorkspace {
     int64_t Tp;  // T padded to whole M tiles
-    size_t hT_off, Wt_off[2], G_off, Gt_off, ctr_off, total;
+    int64_t Vp;  // V padded to whole 64-row k-blocks (rows past V are zeros)
+    size_t W16_off, h16_off, G_off, ctr_off, total;
     int64_t n_chunks;  // vocabulary chunks of VC columns
 };
 static BwdWorkspace bwd_layout(int64_t T, int64_t V, int64_t d) {
     BwdWorkspace w;
     w.Tp = (T + BM - 1) / BM * BM;
-    w.hT_off = 0;                                                 // [d, Tp] fp16
-    w.Wt_off[0] = align_up(w.hT_off + (size_t)d * w.Tp * 2, 1024);  // [d, VC] fp16, two
-    w.Wt_off[1] = align_up(w.Wt_off[0] + (size_t)d * VC * 2, 1024); // (chunks alternate)
-    w.G_off = align_up(w.Wt_off[1] + (size_t)d * VC * 2, 1024);     // [Tp, VC] fp16
-    w.Gt_off = align_up(w.G_off + (size_t)w.Tp * VC * 2, 1024);  // [VC, Tp] fp16
-    w.ctr_off = align_up(w.Gt_off + (size_t)VC * w.Tp * 2, 1024);  // int[n_chunks]
+    w.Vp = (V + BK - 1) / BK * BK;
+    w.W16_off = 0;                                                   // [Vp, d] fp16
+    w.h16_off = align_up(w.W16_off + (size_t)w.Vp * d * 2, 1024);    // [Tp, d] fp16
+    w.G_off = align_up(w.h16_off + (size_t)w.Tp * d * 2, 1024);      // [Tp, VC] fp16
+    w.ctr_off = align_up(w.G_off + (size_t)w.Tp * VC * 2, 1024);     // int[n_chunks]
     w.n_chunks = (V + VC - 1) / VC;
     w.total = align_up(w.ctr_off + (size_t)w.n_chunks * sizeof(int), 1024);
     return w;
@@ -916,22 +1037,23 @@ int pstat_lmhead_backward(const void* hidden, const void* W, int64_t T, int64_t 
     if (rc != PSTAT_OK) return rc;
 
     char* ws = static_cast<char*>(workspace);
-    __half* hT = reinterpret_cast<__half*>(ws + wl.hT_off);
-    __half* Wt[2] = {reinterpret_cast<__half*>(ws + wl.Wt_off[0]),
-                     reinterpret_cast<__half*>(ws + wl.Wt_off[1])};
+    __half* W16 = reinterpret_cast<__half*>(ws + wl.W16_off);
+    __half* h16 = reinterpret_cast<__half*>(ws + wl.h16_off);
     __half* G = reinterpret_cast<__half*>(ws + wl.G_off);
-    __half* Gt = reinterpret_cast<__half*>(ws + wl.Gt_off);
     const int64_t Tp = wl.Tp;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
-    CUtensorMap map_h, map_w, map_G, map_Wt[2], map_Gt, map_hT;
+    // K-major maps (inner coordinate K): hidden and W for the recompute, G for
+    // dhidden.  MN-major maps (inner coordinate M or N): G for dW (inner =
+    // vocabulary), W16 for dhidden (inner = d) and h' for dW (inner = d).
+    constexpr int kAccTM = lm::TileCfg<lm::ACC_WIDE>::TM;  // A rows per accumulation tile
+    CUtensorMap map_h, map_w, map_G, map_Gmn, map_W16, map_h16;
     if (!lm::make_map(&map_h, false, hidden, T, d, d, lm::BM) ||
         !lm::make_map(&map_w, false, W, V, d, d, lm::BN) ||
-        !lm::make_map(&map_G, true, G, Tp, lm::VC, lm::VC, lm::BM) ||
-        !lm::make_map(&map_Wt[0], true, Wt[0], d, lm::VC, lm::VC, lm::BN) ||
-        !lm::make_map(&map_Wt[1], true, Wt[1], d, lm::VC, lm::VC, lm::BN) ||
-        !lm::make_map(&map_Gt, true, Gt, lm::VC, Tp, Tp, lm::BM) ||
-        !lm::make_map(&map_hT, true, hT, d, Tp, Tp, lm::BN))
+        !lm::make_map(&map_G, true, G, Tp, lm::VC, lm::VC, kAccTM) ||
+        !lm::make_map_mn4d(&map_Gmn, G, Tp, lm::VC, lm::VC, kAccTM) ||
+        !lm::make_map_mn4d(&map_W16, W16, wl.Vp, d, d, lm::BN) ||
+        !lm::make_map_mn4d(&map_h16, h16, Tp, d, d, lm::BN))
         return PSTAT_ERR_CUDA;
 
     lm::GradEpi ge;
@@ -943,84 +1065,61 @@ int pstat_lmhead_backward(const void* hidden, const void* W, int64_t T, int64_t 
     ge.rowstats = reinterpret_cast<const float2*>(rowstats);
     ge.G = G;
     ge.ldg = lm::VC;
-    ge.Gt = Gt;
-    ge.ldgt = Tp;
     ge.dev_error = dev_error;
 
     const int64_t n_chunks = wl.n_chunks;
     int* ctr = reinterpret_cast<int*>(ws + wl.ctr_off);  // one unit counter per chunk
     if (cudaMemsetAsync(ctr, 0, (size_t)n_chunks * sizeof(int), st) != cudaSuccess)
         return PSTAT_ERR_CUDA;
-
-    // The transposes (hidden once, W_c per chunk into alternating buffers) run
-    // on a side stream: W_{c+1} is transposed while chunk c's GEMMs run, after
-    // the GEMMs of chunk c-1 (the last reader of its buffer) are done.
-    lm::SideStream x;
-    if (!x.ok) return PSTAT_ERR_CUDA;
-    auto transpose_w = [&](int64_t c) {
-        const int64_t c0 = c * lm::VC;
-        const int64_t vc = (V - c0) < lm::VC ? (V - c0) : lm::VC;
-        // W_c^T (fp16; vocabulary columns past the chunk end as zeros)
-        return lm::launch_transpose(static_cast<const uint16_t*>(W) + c0 * d, vc, d, d,
-                                    Wt[c & 1], lm::VC, lm::VC, dev_error, x.s);
-    };
-    if (!x.fork(st)) return PSTAT_ERR_CUDA;
-    // hidden^T once (fp16, tokens padded to Tp with zeros)
-    if (lm::launch_transpose(static_cast<const uint16_t*>(hidden), T, d, d, hT, Tp, Tp, dev_error,
-                             x.s) != cudaSuccess ||
-        cudaEventRecord(x.hT, x.s) != cudaSuccess || transpose_w(0) != cudaSuccess ||
-        cudaEventRecord(x.tr[0], x.s) != cudaSuccess)
+    // 0. W16 = fp16(W), h' = fp16(w hidden)
+    if (lm::launch_to_fp16(W, V, wl.Vp, hidden, weights, T, Tp, d, W16, h16, dev_error,
+                           dev.sm_count, st) != cudaSuccess)
         return PSTAT_ERR_CUDA;
 
     for (int64_t c = 0; c < n_chunks; ++c) {
         const int64_t c0 = c * lm::VC;
         const int64_t vc = (V - c0) < lm::VC ? (V - c0) : lm::VC;
-        const int b = (int)(c & 1);
-        if (c + 1 < n_chunks) {
-            if (c >= 1 && cudaStreamWaitEvent(x.s, x.acc[b ^ 1], 0) != cudaSuccess)
-                return PSTAT_ERR_CUDA;
-            if (transpose_w(c + 1) != cudaSuccess ||
-                cudaEventRecord(x.tr[b ^ 1], x.s) != cudaSuccess)
-                return PSTAT_ERR_CUDA;
-        }
-        // 1. recompute the chunk's logits -> G, Gt
+        // 1. recompute the chunk's logits -> G = fp16(2^15 q)
         ge.c0 = c0;
         const lm::GemmGeo g1 = lm::geo(Tp, vc, d, 1, c0);
         if (lm::launch_gemm<lm::GradEpi, false>(map_h, map_w, g1, ge, dev_error, dev.sm_count,
                                                 st) != cudaSuccess)
             return PSTAT_ERR_CUDA;
-        if (cudaStreamWaitEvent(st, x.tr[b], 0) != cudaSuccess ||
-            (c == 0 && cudaStreamWaitEvent(st, x.hT, 0) != cudaSuccess))
-            return PSTAT_ERR_CUDA;
-        // 2. dhidden += G W_c  and  3. dW[c0 : c0 + vc] += Gt hidden, in one
-        // launch: CTAs claim units of both GEMMs (the longer-K one first)
-        // from this chunk's counter, so neither leaves a partial last wave.
+        // 2. dhidden += (w 2^-15) G W16_c  and  3. dW[c0 : c0 + vc] += 2^-15 G^T h',
+        // in one launch: CTAs claim units of both GEMMs (the longer-K one
+        // first) from this chunk's counter, so neither leaves a partial last
+        // wave.
         lm::AccumEpi e2;
         e2.out = dhidden;
         e2.ld = d;
         e2.row0 = 0;
         e2.rows = T;
         e2.cols = d;
-        const lm::GemmGeo g2 = lm::geo(T, d, vc, 1, 0, lm::ACC_M_GROUP);
+        e2.row_scale = weights;
+        e2.scale = lm::GRAD_UNSCALE;
+        const lm::GemmGeo g2 = lm::geo(T, d, vc, 1, 0, lm::ACC_M_GROUP, c0, kAccTM);
         lm::AccumEpi e3;
         e3.out = dW;
         e3.ld = d;
         e3.row0 = c0;
         e3.rows = vc;
         e3.cols = d;
-        const lm::GemmGeo g3 = lm::geo(vc, d, Tp, 1, 0, lm::ACC_M_GROUP);
+        e3.row_scale = nullptr;
+        e3.scale = lm::GRAD_UNSCALE;
+        const lm::GemmGeo g3 = lm::geo(vc, d, Tp, 1, 0, lm::ACC_M_GROUP, 0, kAccTM);
+        // dW: A and B MN-major; dhidden: A K-major, B MN-major
+        constexpr uint32_t kDwFirst = lm::layout_bits(1, 1, 0, 1);
+        constexpr uint32_t kDhFirst = lm::layout_bits(0, 1, 1, 1);
         const cudaError_t e =
             g3.k_blocks >= g2.k_blocks
-                ? lm::launch_gemm_pair<lm::AccumEpi, true>(map_Gt, map_hT, g3, e3, map_G,
-                                                           map_Wt[b], g2, e2, ctr + c, dev_error,
-                                                           dev.sm_count, st)
-                : lm::launch_gemm_pair<lm::AccumEpi, true>(map_G, map_Wt[b], g2, e2, map_Gt,
-                                                           map_hT, g3, e3, ctr + c, dev_error,
-                                                           dev.sm_count, st);
-        if (e != cudaSuccess || cudaEventRecord(x.acc[b], st) != cudaSuccess)
-            return PSTAT_ERR_CUDA;
+                ? lm::launch_gemm_pair<lm::AccumEpi, true, kDwFirst, lm::ACC_WIDE>(
+                      map_Gmn, map_h16, g3, e3, map_G, map_W16, g2, e2, ctr + c, dev_error,
+                      dev.sm_count, st)
+                : lm::launch_gemm_pair<lm::AccumEpi, true, kDhFirst, lm::ACC_WIDE>(
+                      map_G, map_W16, g2, e2, map_Gmn, map_h16, g3, e3, ctr + c, dev_error,
+                      dev.sm_count, st);
+        if (e != cudaSuccess) return PSTAT_ERR_CUDA;
     }
-    // x joins the side stream back into st as it goes out of scope
     return PSTAT_OK;
 }
 

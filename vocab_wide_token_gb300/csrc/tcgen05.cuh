@@ -78,6 +78,23 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t smem_addr) {
            | ((uint64_t)2 << 61);                   // 128-byte swizzle
 }
 
+// Shared-memory matrix descriptor for an MN-major operand (its M or N index
+// contiguous) written by TMA as boxes of 64 MN elements (128 bytes) x K rows
+// with the 128-byte swizzle: one 8-row K group is a 1024-byte swizzle atom,
+// the next K group follows at +1024 bytes (stride byte offset), and the next
+// 64 MN elements sit `mn_stride` bytes further (leading byte offset, here the
+// size of one box).  An MMA with K = 16 spans two K groups; successive K
+// steps start 16 rows = 2048 bytes apart, so every start address is atom
+// aligned.
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t smem_addr, uint32_t mn_stride,
+                                                        uint32_t k_stride = 1024) {
+    return (uint64_t)((smem_addr >> 4) & 0x3FFFu)          // start address
+           | ((uint64_t)((mn_stride >> 4) & 0x3FFFu) << 16)  // leading byte offset (MN)
+           | ((uint64_t)((k_stride >> 4) & 0x3FFFu) << 32)   // stride byte offset (K)
+           | ((uint64_t)1 << 46)                            // descriptor version
+           | ((uint64_t)2 << 61);                           // 128-byte swizzle
+}
+
 // ---- tensor memory -> registers ------------------------------------------------
 // Each thread of a warp reads 32 consecutive 32-bit columns of its own lane
 // (the warp's lane quadrant is fixed by its warp index modulo 4).
@@ -110,6 +127,16 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+// 4-D tile load (coordinates innermost first, x a multiple of 16 bytes).
+__device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* map, int x, int y,
+                                            int z, int w, uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w),
+        "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
