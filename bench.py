@@ -8,9 +8,12 @@ logits); the same workload through pstat_forward + pstat_backward is timed in
 the same run under `two_call`, with each kernel's bandwidth.
 
 Prints ONE JSON line (rank 0).  `value` is whole-job tokens/s with inputs
-resident in HBM; `e2e` is the same metric through the Python/C-ABI calls with
-the inputs copied from pinned host memory and logprob/entropy copied back
-inside the timed region; `roofline` is the dominant kernel's algorithmic
+resident in HBM, over R back-to-back blocks of `--steps` steps (R sized so
+the timed region lasts at least a second); `e2e` is the same metric through
+the Python/C-ABI calls with the inputs copied from pinned host memory and
+logprob/entropy copied back inside the timed region (dlogits stays on the
+device), `e2e_dlogits_to_host` the same with the dlogits copied back to
+pinned host memory as well; `roofline` is the dominant kernel's algorithmic
 bytes per launch over its CUDA-event duration against the measured HBM copy
 bandwidth; `cpu_baseline` times the float64 oracle on the host cores over a
 bounded sample of the same workload.
@@ -27,6 +30,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -39,6 +43,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "tokens/s and HBM GB/s (% of roofline) for logprob+entropy+bwd at V=151936"
 V = 151936
+MIN_REGION_S = 1.0  # each timed region lasts at least this long
 
 
 def parse():
@@ -282,10 +287,24 @@ def main():
         torch.cuda.synchronize()
 
     # ---- timed regions: device-resident inputs --------------------------------
-    # (a) the two calls, with events around each; (b) the fused single pass.
+    # Each timed region is R back-to-back blocks of K steps, R chosen by an
+    # untimed pilot block so that a region lasts at least MIN_REGION_S (the
+    # clock sampler then holds at least ~10 samples of it).  (a) the two
+    # calls, with events around each; (b) the fused single pass.
     stream = torch.cuda.current_stream(dev)
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    pa = torch.cuda.Event(enable_timing=True)
+    pb = torch.cuda.Event(enable_timing=True)
+    barrier()
+    pa.record(stream)
+    for _ in range(K):
+        fused()
+    pb.record(stream)
+    barrier()
+    R = max(1, math.ceil(MIN_REGION_S * 1e3 / max(pa.elapsed_time(pb), 1e-3)))
+    R = int(max_over_ranks(R, dev))
+    N = R * K
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(N)]
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -294,7 +313,7 @@ def main():
     start_a = torch.cuda.Event(enable_timing=True)
     end_a = torch.cuda.Event(enable_timing=True)
     start_a.record(stream)
-    for k in range(K):
+    for k in range(N):
         ev[k][0].record(stream)
         pstat.forward(z, y, -100, None, out=(lp, ent, rs), workspace=ws, dev_error=err)
         ev[k][1].record(stream)
@@ -302,14 +321,14 @@ def main():
         ev[k][2].record(stream)
     end_a.record(stream)
     barrier()
-    evb = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    evb = [torch.cuda.Event(enable_timing=True) for _ in range(N + 1)]
     start_b = torch.cuda.Event(enable_timing=True)
     end_b = torch.cuda.Event(enable_timing=True)
     start_b.record(stream)
-    for k in range(K):
+    for k in range(N):
         evb[k].record(stream)
         pstat.forward_backward(z, y, w, -100, out=(lp, ent, rs), dlogits=g, dev_error=err)
-    evb[K].record(stream)
+    evb[N].record(stream)
     end_b.record(stream)
     barrier()
     t_wall1 = time.time()
@@ -318,9 +337,9 @@ def main():
     clocks.stop()
     ms_a = max_over_ranks(start_a.elapsed_time(end_a), dev)
     ms_b = max_over_ranks(start_b.elapsed_time(end_b), dev)
-    fwd_ms = sum(ev[k][0].elapsed_time(ev[k][1]) for k in range(K)) / K
-    bwd_ms = sum(ev[k][1].elapsed_time(ev[k][2]) for k in range(K)) / K
-    fused_ms = sum(evb[k].elapsed_time(evb[k + 1]) for k in range(K)) / K
+    fwd_ms = sum(ev[k][0].elapsed_time(ev[k][1]) for k in range(N)) / N
+    bwd_ms = sum(ev[k][1].elapsed_time(ev[k][2]) for k in range(N)) / N
+    fused_ms = sum(evb[k].elapsed_time(evb[k + 1]) for k in range(N)) / N
     assert err.item() == 0, f"device error bits {err.item()}"
 
     # Algorithmic bytes.  Two calls: the forward reads every row; the backward
@@ -340,58 +359,75 @@ def main():
     roof = {"bound": "hbm", "kernel": "fwdbwd_kernel", "achieved": fused_gbs, "peak": hbm,
             "unit": "GB/s", "frac": fused_gbs / hbm, "peak_kind": peak_kind, "traffic": traffic,
             "algorithmic_bytes_per_launch": fused_bytes}
-    ms_step = ms_b / K
-    tok_s = whole_job_rate(T, K, world, ms_b)
+    ms_step = ms_b / N
+    tok_s = whole_job_rate(T, N, world, ms_b)
 
     line = {
         "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "timed_blocks": R, "timed_steps": N,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": arm_config(T, world),
         "gbs": fused_gbs,
         "roofline": roof,
-        "gpu_launches": K,
+        "gpu_launches": N,
         "two_call": {"step": "pstat_forward + pstat_backward",
-                     "value": whole_job_rate(T, K, world, ms_a), "ms_per_step": ms_a / K,
-                     "gbs": (fwd_bytes + bwd_bytes) / (ms_a / K / 1e3) / 1e9,
+                     "value": whole_job_rate(T, N, world, ms_a), "ms_per_step": ms_a / N,
+                     "gbs": (fwd_bytes + bwd_bytes) / (ms_a / N / 1e3) / 1e9,
                      "forward_ms": fwd_ms, "forward_gbs": fwd_gbs, "forward_frac": fwd_gbs / hbm,
                      "backward_ms": bwd_ms, "backward_gbs": bwd_gbs,
                      "backward_frac": bwd_gbs / hbm, "active_rows": active_rows,
-                     "gpu_launches": 2 * K},
+                     "gpu_launches": 2 * N},
         "clocks": clocks.summary(),
     }
 
     # ---- e2e: host buffers through the public API ---------------------------
+    # Inputs come from pinned host memory every step.  `e2e`: logprob and
+    # entropy are read back; dlogits stays in device memory, where the
+    # trainer's next backward step consumes it.  `e2e_dlogits_to_host`: the
+    # bf16 dlogits are copied back to pinned host memory as well, block by
+    # block as the kernel finishes each.
     if not args.no_e2e:
         zh = z.cpu().pin_memory()
         yh = y.cpu().pin_memory()
         wh = w.cpu().pin_memory()
         outh = torch.empty(2, T, dtype=torch.float32).pin_memory()
+        gh = torch.empty(T, V, dtype=torch.bfloat16).pin_memory()
         Ke = min(K, 20)
+        h2d = zh.numel() * 2 + yh.numel() * 8 + wh.numel() * 4
 
-        def e2e_step():
+        def e2e_step(dlogits_host=None):
             # host logits, labels, weights -> device results, the row blocks'
             # copies overlapping the kernel on the previous block
             pstat.forward_backward_from_host(zh, yh, wh, -100, device=dev, out=(lp, ent, rs),
-                                             dlogits=g, dev_error=err)
+                                             dlogits=g, dev_error=err,
+                                             dlogits_host=dlogits_host)
             outh[0].copy_(lp, non_blocking=True)
             outh[1].copy_(ent, non_blocking=True)
 
-        for _ in range(2):
-            e2e_step()
-        barrier()
-        s2 = torch.cuda.Event(enable_timing=True)
-        e2 = torch.cuda.Event(enable_timing=True)
-        s2.record(stream)
-        for _ in range(Ke):
-            e2e_step()
-        e2.record(stream)
-        barrier()
-        ms2 = max_over_ranks(s2.elapsed_time(e2), dev)
+        def timed_e2e(dlogits_host):
+            for _ in range(2):
+                e2e_step(dlogits_host)
+            barrier()
+            s2 = torch.cuda.Event(enable_timing=True)
+            e2 = torch.cuda.Event(enable_timing=True)
+            s2.record(stream)
+            for _ in range(Ke):
+                e2e_step(dlogits_host)
+            e2.record(stream)
+            barrier()
+            return max_over_ranks(s2.elapsed_time(e2), dev)
+
+        ms2 = timed_e2e(None)
         line["e2e"] = {"value": whole_job_rate(T, Ke, world, ms2), "unit": "tokens/s",
-                       "h2d_bytes_per_step": zh.numel() * 2 + yh.numel() * 8 + wh.numel() * 4,
-                       "d2h_bytes_per_step": outh.numel() * 4, "steps": Ke}
-        del zh
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": outh.numel() * 4,
+                       "steps": Ke, "dlogits": "stays in device memory"}
+        ms3 = timed_e2e(gh)
+        line["e2e_dlogits_to_host"] = {
+            "value": whole_job_rate(T, Ke, world, ms3), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": outh.numel() * 4 + gh.numel() * 2,
+            "steps": Ke, "dlogits": "copied to pinned host memory inside the timed region"}
+        del zh, gh
 
     # ---- fused lm_head variant (rank 0 reports) ------------------------------
     if not args.no_lmhead:

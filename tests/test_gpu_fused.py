@@ -259,3 +259,10 @@ def test_from_host_equals_device_call(cuda_lib, T, block):
     torch.cuda.synchronize()
     for a, b, name in zip(ref, got, ("logprob", "entropy", "rowstats", "dlogits")):
         assert torch.equal(_bits(a), _bits(b)), name
+    # the same with dlogits also copied back to pinned host memory block by block
+    gh = torch.full((T, V), float("nan"), dtype=torch.bfloat16).pin_memory()
+    got2 = cuda_lib.forward_backward_from_host(zh, yh, wh, IGN, block_rows=block,
+                                               dlogits_host=gh)
+    torch.cuda.current_stream().synchronize()
+    assert torch.equal(_bits(gh), _bits(ref[3].cpu()))
+    assert torch.equal(_bits(got2[0]), _bits(ref[0]))

@@ -414,25 +414,32 @@ def backward_shard(logits: torch.Tensor, labels: torch.Tensor | None,
 _side_streams: dict = {}
 
 
-def _side_stream(device: torch.device) -> torch.cuda.Stream:
-    s = _side_streams.get(device)
+def _side_stream(device: torch.device, role: str = "h2d") -> torch.cuda.Stream:
+    """A stream per device and role, created on first use and kept."""
+    s = _side_streams.get((device, role))
     if s is None:
         s = torch.cuda.Stream(device=device)
-        _side_streams[device] = s
+        _side_streams[(device, role)] = s
     return s
 
 
 def forward_backward_from_host(logits: torch.Tensor, labels: torch.Tensor | None,
                                weights: torch.Tensor | None, ignore_index: int = -100, *,
                                device=None, out_dtype: torch.dtype | None = None,
-                               block_rows: int = 1024, out=None, dlogits=None, dev_error=None):
+                               block_rows: int = 1024, out=None, dlogits=None, dev_error=None,
+                               dlogits_host: torch.Tensor | None = None):
     """forward_backward on logits, labels and weights that live in host memory
     (pinned, for the copies to run asynchronously).  Row blocks of the logits
     are copied into a double-buffered device staging area on a side stream
     while pstat_forward_backward runs on the previous block on the current
     stream, so after the last copy only one block's kernel remains.  Returns
     device (logprob, entropy, rowstats, dlogits), complete in stream order on
-    the current stream."""
+    the current stream.
+
+    With `dlogits_host` (a pinned host [T, V] tensor of the output dtype),
+    each block's dlogits is also copied back to it on a second side stream
+    as soon as its kernel has run, overlapping the next blocks' copies in and
+    kernels; the current stream waits for the last of these copies."""
     if logits.is_cuda or logits.dim() != 2 or not logits.is_contiguous():
         raise ValueError("logits must be a contiguous 2-D host tensor")
     T, V = logits.shape
@@ -453,8 +460,13 @@ def forward_backward_from_host(logits: torch.Tensor, labels: torch.Tensor | None
     lp, ent, rs = out
     if dlogits is None:
         dlogits = torch.empty(T, V, dtype=out_dtype, device=dev)
+    if dlogits_host is not None and (dlogits_host.is_cuda or dlogits_host.dtype != dlogits.dtype
+                                     or tuple(dlogits_host.shape) != (T, V)
+                                     or not dlogits_host.is_contiguous()):
+        raise ValueError("dlogits_host must be a contiguous host tensor [T, V] of the output dtype")
     if T == 0:
         return lp, ent, rs, dlogits
+    back = _side_stream(dev, "d2h") if dlogits_host is not None else None
     B = min(block_rows, T)
     bufs = [torch.empty(B, V, dtype=logits.dtype, device=dev) for _ in range(2)]
     for b in bufs:
@@ -479,6 +491,15 @@ def forward_backward_from_host(logits: torch.Tensor, labels: torch.Tensor | None
                          dlogits=dlogits[r0:r1], dev_error=dev_error)
         freed[i % 2] = torch.cuda.Event()
         freed[i % 2].record(cur)
+        if back is not None:
+            back.wait_event(freed[i % 2])
+            with torch.cuda.stream(back):
+                dlogits_host[r0:r1].copy_(dlogits[r0:r1], non_blocking=True)
+    if back is not None:
+        done = torch.cuda.Event()
+        done.record(back)
+        cur.wait_event(done)
+        dlogits.record_stream(back)
     return lp, ent, rs, dlogits
 
 
