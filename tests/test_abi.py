@@ -13,6 +13,13 @@ HEADER = os.path.join(ROOT, "include", "pstat.h")
 
 
 def _load():
+    # PSTAT_TEST_LIB names another build of the library to check (the
+    # sanitizer build, see test_abi_sanitized.py).
+    path = os.environ.get("PSTAT_TEST_LIB")
+    if path:
+        from vocab_wide_token_gb300 import pstat
+
+        return pstat.declare_prototypes(ctypes.CDLL(path))
     from vocab_wide_token_gb300 import build
 
     if not os.path.exists(build.LIB):

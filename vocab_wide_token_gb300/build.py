@@ -31,9 +31,18 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libpstat.so")
 
 
-def _compile(src: str, verbose: bool) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src).replace(".cu", ".o"))
-    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+# Host-side instrumentation for the sanitizer build (AddressSanitizer and
+# UndefinedBehaviorSanitizer on the C-ABI layer's host code; device code is
+# unaffected).  Errors are fatal, so a test run fails on the first one.
+# (nvcc splits -Xcompiler values at commas, so each flag is passed alone.)
+SANITIZE_FLAGS = ["-Xcompiler", "-fsanitize=address", "-Xcompiler", "-fsanitize=undefined",
+                  "-Xcompiler", "-fno-sanitize-recover=all", "-Xcompiler", "-fno-omit-frame-pointer",
+                  "-g"]
+
+
+def _compile(src: str, verbose: bool, out_dir: str = BUILD, extra=()) -> str:
+    obj = os.path.join(out_dir, os.path.basename(src).replace(".cu", ".o"))
+    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -59,6 +68,32 @@ def build(verbose: bool = False) -> str:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
     return LIB
+
+
+def build_sanitized() -> str:
+    """The same library with SANITIZE_FLAGS on its host code, at
+    _build/sanitize/libpstat_sanitized.so, for the host-side tests (load it
+    with the sanitizer runtimes preloaded).  Rebuilt when a source is newer."""
+    out_dir = os.path.join(BUILD, "sanitize")
+    lib = os.path.join(out_dir, "libpstat_sanitized.so")
+    sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    deps = sources + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) \
+        + glob.glob(os.path.join(INCLUDE, "*.h"))
+    if os.path.exists(lib) and os.path.getmtime(lib) >= max(os.path.getmtime(d) for d in deps):
+        return lib
+    os.makedirs(out_dir, exist_ok=True)
+    with cf.ThreadPoolExecutor(max_workers=min(8, len(sources))) as ex:
+        objs = list(ex.map(lambda src: _compile(src, False, out_dir, SANITIZE_FLAGS), sources))
+    tmp = lib + f".tmp{os.getpid()}"
+    cuda_lib = os.path.join(os.path.dirname(os.path.dirname(nvcc())), "lib64")
+    cmd = [nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
+           "-Xcompiler", "-fsanitize=address", "-Xcompiler", "-fsanitize=undefined",
+           "-Xlinker", f"-rpath,{cuda_lib}"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -26,48 +26,58 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 # ---- C ABI prototypes -------------------------------------------------------
 _i64, _i32, _vp, _sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
-_lib.pstat_status_string.argtypes = [_i32]
-_lib.pstat_status_string.restype = ctypes.c_char_p
-_lib.pstat_version.restype = _i32
-_lib.pstat_workspace_size.argtypes = [_i64, _i64, _i32, _vp, _i32, ctypes.POINTER(_sz)]
-_lib.pstat_workspace_size.restype = _i32
-_lib.pstat_forward.argtypes = [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _i32, _vp, _vp, _vp,
-                               _vp, _sz, _vp, _vp]
-_lib.pstat_forward.restype = _i32
-_lib.pstat_forward_noalloc.argtypes = [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _i32, _vp,
-                                       _vp, _vp, _vp, _vp]
-_lib.pstat_forward_noalloc.restype = _i32
-_lib.pstat_backward.argtypes = [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _vp,
-                                _i32, _i64, _vp, _sz, _vp, _vp]
-_lib.pstat_backward.restype = _i32
-_lib.pstat_forward_backward.argtypes = [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _i32,
-                                        _vp, _vp, _vp, _vp, _i32, _i64, _vp, _vp]
-_lib.pstat_forward_backward.restype = _i32
-_lib.pstat_log_softmax.argtypes = [_vp, _i32, _i64, _i64, _i64, _vp, _vp, _i32, _vp, _i32, _i64,
-                                   _vp, _sz, _vp, _vp]
-_lib.pstat_log_softmax.restype = _i32
-_lib.pstat_logprob_diff_metrics.argtypes = [_vp, _vp, _vp, _i64, _i64, _vp, _vp]
-_lib.pstat_logprob_diff_metrics.restype = _i32
-_lib.pstat_clipped_surrogate.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_float,
-                                         ctypes.c_float, ctypes.c_float, _vp, _vp, _vp]
-_lib.pstat_clipped_surrogate.restype = _i32
-_lib.pstat_lmhead_workspace_size.argtypes = [_i64, _i64, _i64, ctypes.POINTER(_sz)]
-_lib.pstat_lmhead_workspace_size.restype = _i32
-_lib.pstat_lmhead_fused.argtypes = [_vp, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _vp,
-                                    _sz, _vp, _vp]
-_lib.pstat_lmhead_fused.restype = _i32
-_lib.pstat_lmhead_backward.argtypes = [_vp, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _vp,
-                                       _vp, _sz, _vp, _vp]
-_lib.pstat_lmhead_backward.restype = _i32
-_lib.pstat_shard_stats.argtypes = [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _vp, _vp]
-_lib.pstat_shard_stats.restype = _i32
-_lib.pstat_combine_shards.argtypes = [_vp, _i64, _i32, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp]
-_lib.pstat_combine_shards.restype = _i32
-_lib.pstat_backward_shard.argtypes = [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _i64,
-                                      _i64, _vp, _i32, _i64, _vp, _vp]
-_lib.pstat_backward_shard.restype = _i32
-_lib.pstat_noalloc_scratch_bytes.argtypes = []
-_lib.pstat_noalloc_scratch_bytes.restype = _sz
+
+
+def declare_prototypes(lib: ctypes.CDLL) -> ctypes.CDLL:
+    """Set the argument and result types of every entry point of
+    include/pstat.h on a loaded copy of the library (ctypes would otherwise
+    pass 64-bit sizes as C ints)."""
+    lib.pstat_status_string.argtypes = [_i32]
+    lib.pstat_status_string.restype = ctypes.c_char_p
+    lib.pstat_version.restype = _i32
+    lib.pstat_workspace_size.argtypes = [_i64, _i64, _i32, _vp, _i32, ctypes.POINTER(_sz)]
+    lib.pstat_workspace_size.restype = _i32
+    lib.pstat_forward.argtypes = [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _i32, _vp, _vp, _vp,
+                                  _vp, _sz, _vp, _vp]
+    lib.pstat_forward.restype = _i32
+    lib.pstat_forward_noalloc.argtypes = [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _i32, _vp,
+                                          _vp, _vp, _vp, _vp]
+    lib.pstat_forward_noalloc.restype = _i32
+    lib.pstat_backward.argtypes = [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _i32, _vp,
+                                   _i32, _i64, _vp, _sz, _vp, _vp]
+    lib.pstat_backward.restype = _i32
+    lib.pstat_forward_backward.argtypes = [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _i32,
+                                           _vp, _vp, _vp, _vp, _i32, _i64, _vp, _vp]
+    lib.pstat_forward_backward.restype = _i32
+    lib.pstat_log_softmax.argtypes = [_vp, _i32, _i64, _i64, _i64, _vp, _vp, _i32, _vp, _i32, _i64,
+                                      _vp, _sz, _vp, _vp]
+    lib.pstat_log_softmax.restype = _i32
+    lib.pstat_logprob_diff_metrics.argtypes = [_vp, _vp, _vp, _i64, _i64, _vp, _vp]
+    lib.pstat_logprob_diff_metrics.restype = _i32
+    lib.pstat_clipped_surrogate.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, ctypes.c_float,
+                                            ctypes.c_float, ctypes.c_float, _vp, _vp, _vp]
+    lib.pstat_clipped_surrogate.restype = _i32
+    lib.pstat_lmhead_workspace_size.argtypes = [_i64, _i64, _i64, ctypes.POINTER(_sz)]
+    lib.pstat_lmhead_workspace_size.restype = _i32
+    lib.pstat_lmhead_fused.argtypes = [_vp, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _vp,
+                                       _sz, _vp, _vp]
+    lib.pstat_lmhead_fused.restype = _i32
+    lib.pstat_lmhead_backward.argtypes = [_vp, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _vp, _vp,
+                                          _vp, _sz, _vp, _vp]
+    lib.pstat_lmhead_backward.restype = _i32
+    lib.pstat_shard_stats.argtypes = [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _vp, _vp]
+    lib.pstat_shard_stats.restype = _i32
+    lib.pstat_combine_shards.argtypes = [_vp, _i64, _i32, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp]
+    lib.pstat_combine_shards.restype = _i32
+    lib.pstat_backward_shard.argtypes = [_vp, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _i64,
+                                         _i64, _vp, _i32, _i64, _vp, _vp]
+    lib.pstat_backward_shard.restype = _i32
+    lib.pstat_noalloc_scratch_bytes.argtypes = []
+    lib.pstat_noalloc_scratch_bytes.restype = _sz
+    return lib
+
+
+declare_prototypes(_lib)
 
 F32, BF16 = 0, 1
 OK = 0
