@@ -90,6 +90,14 @@ constexpr int M_GROUP = 32;        // M tiles sharing the L2-resident slice of A
 // rows of A, as 16 tiles of 128 rows before) were within 1-2% of 4 and 16 and
 // ahead of 32.
 constexpr bool ACC_WIDE = true;
+// Tile configuration of the forward statistics GEMM and of the backward's
+// recompute GEMM.  256-row tiles gave the same bits and no measurable gain
+// there (forward 11.73-11.82 against 11.58-11.89 ms, backward 39.2-40.0
+// against 39.7-39.9 ms, same box): their epilogues are heavier and their K
+// (= d) shorter, so the undoubled accumulator costs what the operand traffic
+// saves.
+constexpr bool FWD_WIDE = false;
+constexpr bool GRAD_WIDE = false;
 constexpr int ACC_M_GROUP = 8;
 constexpr uint32_t B_BYTES = BN * BK * 2;   // 32 KB
 constexpr uint32_t TMEM_COLS = 2 * BN;      // two 128 x 256 fp32 accumulators
@@ -861,8 +869,9 @@ static cudaError_t launch_problems(const Problems<Epi>& P, int* dev_error, int s
     return cudaGetLastError();
 }
 
-// One GEMM, static round-robin schedule, both operands K-major.
-template <class Epi, bool kF16>
+// One GEMM, static round-robin schedule, both operands K-major, tile
+// configuration kWide (the geometry's M tiles must be TileCfg<kWide>::TM rows).
+template <class Epi, bool kF16, bool kWide = false>
 static cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmGeo& g,
                                const Epi& epi, int* dev_error, int sm_count, cudaStream_t st) {
     Problems<Epi> P;
@@ -874,7 +883,7 @@ static cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, con
     P.n0 = g.n_units;
     P.total = g.n_units;
     P.counter = nullptr;
-    return launch_problems<Epi, kF16, 0u, false>(P, dev_error, sm_count, st);
+    return launch_problems<Epi, kF16, 0u, kWide>(P, dev_error, sm_count, st);
 }
 
 // Two GEMMs in one launch, units claimed through `counter` (zeroed before),
@@ -936,7 +945,9 @@ struct BwdWorkspace {
 };
 static BwdWorkspace bwd_layout(int64_t T, int64_t V, int64_t d) {
     BwdWorkspace w;
-    w.Tp = (T + BM - 1) / BM * BM;
+    // whole recompute tiles: a recompute tile writes every G row it covers
+    constexpr int tm = TileCfg<GRAD_WIDE>::TM;
+    w.Tp = (T + tm - 1) / tm * tm;
     w.Vp = (V + BK - 1) / BK * BK;
     w.W16_off = 0;                                                   // [Vp, d] fp16
     w.h16_off = align_up(w.W16_off + (size_t)w.Vp * d * 2, 1024);    // [Tp, d] fp16
@@ -993,7 +1004,8 @@ int pstat_lmhead_fused(const void* hidden, const void* W, int64_t T, int64_t V, 
     if (rc != PSTAT_OK) return rc;
 
     CUtensorMap map_h, map_w;
-    if (!lm::make_map(&map_h, false, hidden, T, d, d, lm::BM) ||
+    constexpr int kFwdTM = lm::TileCfg<lm::FWD_WIDE>::TM;
+    if (!lm::make_map(&map_h, false, hidden, T, d, d, kFwdTM) ||
         !lm::make_map(&map_w, false, W, V, d, d, lm::BN))
         return PSTAT_ERR_CUDA;
     char* ws = static_cast<char*>(workspace);
@@ -1005,9 +1017,10 @@ int pstat_lmhead_fused(const void* hidden, const void* W, int64_t T, int64_t V, 
     epi.ignore_index = ignore_index;
     epi.chunk_stats = reinterpret_cast<float4*>(ws + wl.stats_off);
     epi.target = reinterpret_cast<float*>(ws + wl.target_off);
-    const lm::GemmGeo g = lm::geo(T, V, d, lm::STATS_TILES, 0);
+    const lm::GemmGeo g = lm::geo(T, V, d, lm::STATS_TILES, 0, lm::M_GROUP, 0, kFwdTM);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (lm::launch_gemm<lm::StatsEpi, false>(map_h, map_w, g, epi, dev_error, dev.sm_count, st) !=
+    if (lm::launch_gemm<lm::StatsEpi, false, lm::FWD_WIDE>(map_h, map_w, g, epi, dev_error,
+                                                           dev.sm_count, st) !=
         cudaSuccess)
         return PSTAT_ERR_CUDA;
     if (launch_combine(epi.chunk_stats, plan, nullptr, PSTAT_BF16, T, V, V, labels, ignore_index,
@@ -1048,7 +1061,8 @@ int pstat_lmhead_backward(const void* hidden, const void* W, int64_t T, int64_t 
     // vocabulary), W16 for dhidden (inner = d) and h' for dW (inner = d).
     constexpr int kAccTM = lm::TileCfg<lm::ACC_WIDE>::TM;  // A rows per accumulation tile
     CUtensorMap map_h, map_w, map_G, map_Gmn, map_W16, map_h16;
-    if (!lm::make_map(&map_h, false, hidden, T, d, d, lm::BM) ||
+    constexpr int kGradTM = lm::TileCfg<lm::GRAD_WIDE>::TM;
+    if (!lm::make_map(&map_h, false, hidden, T, d, d, kGradTM) ||
         !lm::make_map(&map_w, false, W, V, d, d, lm::BN) ||
         !lm::make_map(&map_G, true, G, Tp, lm::VC, lm::VC, kAccTM) ||
         !lm::make_map_mn4d(&map_Gmn, G, Tp, lm::VC, lm::VC, kAccTM) ||
@@ -1081,9 +1095,9 @@ int pstat_lmhead_backward(const void* hidden, const void* W, int64_t T, int64_t 
         const int64_t vc = (V - c0) < lm::VC ? (V - c0) : lm::VC;
         // 1. recompute the chunk's logits -> G = fp16(2^15 q)
         ge.c0 = c0;
-        const lm::GemmGeo g1 = lm::geo(Tp, vc, d, 1, c0);
-        if (lm::launch_gemm<lm::GradEpi, false>(map_h, map_w, g1, ge, dev_error, dev.sm_count,
-                                                st) != cudaSuccess)
+        const lm::GemmGeo g1 = lm::geo(Tp, vc, d, 1, c0, lm::M_GROUP, 0, kGradTM);
+        if (lm::launch_gemm<lm::GradEpi, false, lm::GRAD_WIDE>(map_h, map_w, g1, ge, dev_error,
+                                                               dev.sm_count, st) != cudaSuccess)
             return PSTAT_ERR_CUDA;
         // 2. dhidden += (w 2^-15) G W16_c  and  3. dW[c0 : c0 + vc] += 2^-15 G^T h',
         // in one launch: CTAs claim units of both GEMMs (the longer-K one
