@@ -445,10 +445,45 @@ def main():
                                 "kind": "oracle",
                                 "sample": f"{rows} rows of the same workload law (V={V}, bf16), "
                                           "float64 forward+backward, one pass"}
+        line["cpu_baseline"]["parity"] = sample_parity(pstat, oracle, zs, ys, ws_, dev)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def sample_parity(pstat, oracle, zs, ys, ws_, dev):
+    """The headline step on the oracle's sample, against the oracle: the
+    largest logprob and entropy errors, the largest dlogits error beyond the
+    bf16 rule's allowance (<= 0 passes), and a bitwise batch-invariance check
+    of a few rows computed alone against the same rows in the sample batch."""
+    import numpy as np
+    import torch
+
+    z = torch.from_numpy(zs.view("int16")).view(torch.bfloat16).to(dev)
+    y = torch.from_numpy(ys).to(dev)
+    w = torch.from_numpy(ws_).float().to(dev)
+    lp, ent, rs, g = pstat.forward_backward(z, y, w, -100)
+    probes = [0, 1, z.shape[0] // 2, z.shape[0] - 1]
+    alone = [pstat.forward_backward(z[r:r + 1], y[r:r + 1], w[r:r + 1], -100) for r in probes]
+    torch.cuda.synchronize()
+    ref = oracle.forward(zs, ys, -100)
+    gref = oracle.backward(zs, ys, ws_, -100)
+    a = g.double().cpu().numpy()
+    br = torch.from_numpy(gref).to(torch.bfloat16).double().numpy()
+    ax = np.abs(gref)
+    e = np.floor(np.log2(np.maximum(ax, 2.0**-126)))
+    allow = np.maximum(1e-3 * ax, np.maximum(2.0 ** (e - 7), 2.0**-133))
+    bits = lambda t: t.contiguous().view(torch.int16 if t.element_size() == 2 else torch.int32)
+    invariant = all(torch.equal(bits(o[0]), bits(lp[r:r + 1])) and
+                    torch.equal(bits(o[1]), bits(ent[r:r + 1])) and
+                    torch.equal(bits(o[3]), bits(g[r:r + 1]))
+                    for r, o in zip(probes, alone))
+    return {"rows": int(z.shape[0]),
+            "max_abs_logprob_err": float(np.max(np.abs(lp.double().cpu().numpy() - ref["logprob"]))),
+            "max_abs_entropy_err": float(np.max(np.abs(ent.double().cpu().numpy() - ref["entropy"]))),
+            "dlogits_max_excess_over_bf16_rule": float(np.max(np.abs(a - br) - allow)),
+            "batch_invariant_rows": len(probes), "batch_invariant": bool(invariant)}
 
 
 def bench_lmhead(pstat, dev, tflops, tflops_sus, peak_kind, T=16384, steps=3, warmup=1):
