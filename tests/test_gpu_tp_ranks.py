@@ -116,3 +116,48 @@ def test_two_ranks_real_kernels(cuda_lib, tmp_path, dtype, T, V, bounds):
         assert_forward_close(res["lpG"], res["entG"], ref, dtype, what=f"rank {r} gathered")
         assert_grad_close(res["g"][rows], gref[:, b0:b1], dtype, f"rank {r} sharded")
         assert_grad_close(res["gG"][rows], gref[:, b0:b1], dtype, f"rank {r} gathered")
+
+
+def _nccl_rank(index, port, T, V, seed, outdir):
+    import torch.distributed as dist
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), NCCL_NVLS_ENABLE="0")
+    torch.cuda.set_device(0)
+    dist.init_process_group("nccl", rank=0, world_size=1, device_id=torch.device("cuda", 0))
+    try:
+        from vocab_wide_token_gb300 import pstat, tp
+
+        z, y, w = _draw(T, V, torch.bfloat16, seed)
+        err = pstat.new_error_flag(z.device)
+        lp, ent, rs, bounds = tp.tp_forward(z, y, 0, IGN, dev_error=err)
+        g = tp.tp_backward(z, y, w, rs, 0, V, IGN, dev_error=err)
+        lpG, entG, rsG, gG, _ = tp.tp_forward_backward_gather(z, y, w, 0, IGN, dev_error=err)
+        torch.cuda.synchronize()
+        torch.save({"bounds": bounds, "err": int(err.item()), "lp": lp.cpu(), "ent": ent.cpu(),
+                    "rs": rs.cpu(), "g": g.cpu(), "lpG": lpG.cpu(), "gG": gG.contiguous().cpu(),
+                    "on_device": bool(lp.is_cuda and g.is_cuda)},
+                   os.path.join(outdir, "nccl.pt"))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_nccl_branch_single_rank(cuda_lib, tmp_path):
+    """The NCCL branch of the orchestration (collectives on device tensors,
+    no host staging), exercised with one rank holding the whole vocabulary:
+    the results equal the single-process calls bit for bit."""
+    import torch.distributed as dist
+
+    if not dist.is_nccl_available():
+        pytest.skip("NCCL not available")
+    T, V, seed = 96, 20011, 5
+    mp.start_processes(_nccl_rank, args=(_free_port(), T, V, seed, str(tmp_path)), nprocs=1,
+                       join=True, start_method="spawn")
+    res = torch.load(os.path.join(tmp_path, "nccl.pt"))
+    assert res["bounds"] == [0, V] and res["err"] == 0 and res["on_device"]
+    z, y, w = _draw(T, V, torch.bfloat16, seed)
+    lp, ent, rs = cuda_lib.forward(z, y, IGN)
+    g = cuda_lib.backward(z, y, w, rs, IGN)
+    lpF, entF, rsF, gF = cuda_lib.forward_backward(z, y, w, IGN)
+    torch.cuda.synchronize()
+    for key, want in (("lp", lp), ("ent", ent), ("rs", rs), ("g", g), ("lpG", lpF), ("gG", gF)):
+        assert torch.equal(_bits(res[key]), _bits(want.cpu())), key
