@@ -365,6 +365,20 @@ PSTAT_API int pstat_lmhead_backward(const void* hidden, const void* W, int64_t T
                           const float* rowstats, float* dhidden, float* dW, void* workspace,
                           size_t ws_bytes, int* dev_error, pstat_stream_t stream);
 
+/*
+ * Self-test of the bounded waits.  Every kernel of this library waits on its
+ * mbarriers for at most a fixed time (2 s); a wait that runs out sets
+ * PSTAT_DEV_TIMEOUT in *dev_error and the kernel winds down instead of
+ * hanging the GPU.  This entry point runs one such wait, limited to
+ * `limit_ns` nanoseconds (at most 1e9, else PSTAT_ERR_SHAPE), on a barrier
+ * that nothing arrives at, with no copy in flight: afterwards *dev_error
+ * (a device int, required) has PSTAT_DEV_TIMEOUT set and the context is
+ * usable as before.  The pages have no counterpart; it exists to test the
+ * library's failure path without faulting or hanging a GPU.
+ */
+PSTAT_API int pstat_selftest_wait_timeout(uint64_t limit_ns, int* dev_error,
+                                          pstat_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

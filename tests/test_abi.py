@@ -271,3 +271,9 @@ def test_noalloc_scratch_size_matches_header(exports):
     want = int(m.group(1)) << int(m.group(2))
     exports.pstat_noalloc_scratch_bytes.restype = ctypes.c_size_t
     assert exports.pstat_noalloc_scratch_bytes() == want == pstat.NOALLOC_SCRATCH_BYTES
+
+
+def test_selftest_argument_checks(lib):
+    # the device error flag is required; the wait limit is at most one second
+    assert lib.pstat_selftest_wait_timeout(1000, None, None) == -1
+    assert lib.pstat_selftest_wait_timeout(2_000_000_000, ctypes.c_void_p(0x1000), None) == -2

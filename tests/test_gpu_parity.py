@@ -245,3 +245,24 @@ def test_bad_output_tensors_raise_before_launch(cuda_lib):
     lp2, ent2, rs2 = cuda_lib.forward(z, y, IGN)
     torch.cuda.synchronize()
     assert torch.equal(lp, lp2) and torch.equal(ent, ent2)
+
+
+def test_bounded_wait_times_out_and_the_context_stays_usable(cuda_lib):
+    """A kernel's wait on an mbarrier that nothing arrives at gives up after
+    its limit and reports PSTAT_DEV_TIMEOUT instead of hanging; no copy is in
+    flight, and the next calls run normally."""
+    import time
+
+    t0 = time.perf_counter()
+    bits = cuda_lib.selftest_wait_timeout("cuda", 20_000_000)  # 20 ms
+    dt = time.perf_counter() - t0
+    assert bits == cuda_lib.DEV_TIMEOUT
+    assert dt < 5.0
+    z = torch.randn(8, 3000, device="cuda")
+    y = torch.randint(0, 3000, (8,), device="cuda")
+    err = cuda_lib.new_error_flag(z.device)
+    lp, ent, rs = cuda_lib.forward(z, y, -100, dev_error=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    ref = oracle.forward(z.cpu().numpy(), y.cpu().numpy(), -100)
+    assert_forward_close(lp, ent, ref, torch.float32, what="after the timeout self-test")

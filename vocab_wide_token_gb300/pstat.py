@@ -74,6 +74,8 @@ def declare_prototypes(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.pstat_backward_shard.restype = _i32
     lib.pstat_noalloc_scratch_bytes.argtypes = []
     lib.pstat_noalloc_scratch_bytes.restype = _sz
+    lib.pstat_selftest_wait_timeout.argtypes = [ctypes.c_uint64, _vp, _vp]
+    lib.pstat_selftest_wait_timeout.restype = _i32
     return lib
 
 
@@ -636,6 +638,17 @@ def lmhead_backward(hidden, W, labels, weights, rowstats, ignore_index: int = -1
           _ptr(dhidden), _ptr(dW), _ptr(workspace), workspace.numel(), _ptr(dev_error),
           _stream(dev))
     return dhidden, dW
+
+
+def selftest_wait_timeout(device, limit_ns: int = 10_000_000) -> int:
+    """Runs the library's bounded wait on a barrier that nothing arrives at
+    (pstat_selftest_wait_timeout) and returns the device error bits it left:
+    PSTAT_DEV_TIMEOUT when the failure path works."""
+    dev = torch.device(device)
+    flag = new_error_flag(dev)
+    _call(dev, "pstat_selftest_wait_timeout", _lib.pstat_selftest_wait_timeout,
+          int(limit_ns), _ptr(flag), _stream(dev))
+    return int(flag.item())
 
 
 class PolicyStats(torch.autograd.Function):
