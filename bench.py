@@ -489,7 +489,7 @@ def sample_parity(pstat, oracle, zs, ys, ws_, dev):
 def bench_lmhead(pstat, dev, tflops, tflops_sus, peak_kind, T=16384, steps=3, warmup=1):
     """Fused lm_head on hidden [T, 4096] x W [151936, 4096] bf16: the forward
     (tcgen05 GEMM with the statistics epilogue + combine; 2 T V d flops) and
-    the backward (one fp16 conversion of W and w hidden, then per 16384-column
+    the backward (one fp16 conversion of W and w hidden, then per 32768-column
     chunk: recompute GEMM -> fp16 gradient tile, one launch of the dhidden and
     dW GEMMs; 6 T V d flops)."""
     import torch
@@ -539,7 +539,7 @@ def bench_lmhead(pstat, dev, tflops, tflops_sus, peak_kind, T=16384, steps=3, wa
     flop_b = 6.0 * T * V * dm
     af = flop_f / (fwd_ms / 1e3) / 1e12
     ab = flop_b / (bwd_ms / 1e3) / 1e12
-    n_chunks = (V + 16383) // 16384  # vocabulary columns staged per backward chunk
+    n_chunks = (V + 32767) // 32768  # vocabulary columns staged per backward chunk
     return {"status": "ok", "workload": f"hidden [{T}, {dm}] x W [{V}, {dm}] bf16, sampled labels",
             "forward_ms": fwd_ms, "forward_tokens_per_s": T / (fwd_ms / 1e3),
             "backward_ms": bwd_ms, "backward_tokens_per_s": T / (bwd_ms / 1e3),

@@ -13,7 +13,7 @@
 // alone:
 //   0. once per call, W -> W16 = fp16(W) [V, d] and hidden -> h' =
 //      fp16(w_t hidden_t) [T, d] (one memory-bound launch);
-//   per 16384-column vocabulary chunk c:
+//   per 32768-column vocabulary chunk c:
 //   1. recompute the chunk's logits tile by tile and turn them on chip into
 //      G = fp16(2^15 q) [T, Vc] (row-major);
 //   2. dhidden += (w_t 2^-15) (G W16_c)   A = G (K-major), B = W16_c read in
@@ -75,10 +75,13 @@ constexpr int UK = 16;             // K per tcgen05.mma of kind::f16
 // against an average of 500; 8-tile units cap that at 504.
 constexpr int LM_CHUNK = 2048;
 constexpr int STATS_TILES = LM_CHUNK / BN;
-// Backward vocabulary chunk (columns staged as G).  16384 columns give each
-// accumulation launch twice the units of 8192, halving the share of its last
-// partial wave: 38.1-38.6 against 39.2-39.4 ms per backward at T = 16384.
-constexpr int VC = 16384;
+// Backward vocabulary chunk (columns staged as G).  Wider chunks give each
+// accumulation launch more units, so its last partial wave weighs less, and
+// fewer launches: at T = 16384, 8192 columns took 39.2-39.4 ms per backward,
+// 16384 columns 38.1-38.6 ms, and 32768 columns 0.7% less again (same-box
+// A/B, three pairs).  The width is a constant: it fixes the order in which a
+// dhidden element accumulates the chunks.
+constexpr int VC = 32768;
 // G holds 2^15 q, q = onehot(y) - p in [-1, 1]: no |q| >= 2^-29 is subnormal
 // in fp16 and |2^15 q| <= 32768 < 65504.
 constexpr float GRAD_SCALE = 32768.f;
