@@ -53,7 +53,7 @@ int device_info(DeviceInfo* info);  // PSTAT_OK / PSTAT_ERR_CUDA / PSTAT_ERR_UNS
 constexpr int kMaxDevices = 64;
 
 // Id of the context current on this thread; 0 when none is current yet or
-// the driver cannot report it (callers then redo their set-up every time).
+// the CUDA driver cannot report it (callers then redo their set-up every time).
 uint64_t current_context_id();
 
 // For each device, the id of the context in which a one-time set-up last ran.

@@ -1,7 +1,7 @@
 // pstat_api.cu -- the extern "C" entry points of libpstat.so: argument
 // checks, workspace layout and kernel launches on the caller's stream.
 // Contracts are documented in include/pstat.h.
-#include <cuda.h>  // CUcontext, CUresult (types only; the driver is reached by entry point)
+#include <cuda.h>  // CUcontext, CUresult (types only; the CUDA driver is reached by entry point)
 #include <cuda_runtime.h>
 
 #include <cstdint>

@@ -3,7 +3,7 @@
 // allocation and loads, and tiled TMA loads (cp.async.bulk.tensor).
 #pragma once
 
-#include <cuda.h>  // CUtensorMap (type only; no driver symbols are linked)
+#include <cuda.h>  // CUtensorMap (type only; no CUDA driver symbols are linked)
 
 #include <cstdint>
 
