@@ -15,10 +15,10 @@
 //      fp16(w_t hidden_t) [T, d] (one memory-bound launch);
 //   per 32768-column vocabulary chunk c:
 //   1. recompute the chunk's logits tile by tile and turn them on chip into
-//      G = fp16(2^15 q) [T, Vc] (row-major);
-//   2. dhidden += (w_t 2^-15) (G W16_c)   A = G (K-major), B = W16_c read in
+//      G = fp16(-2^15 q) [T, Vc] (row-major; the sign is the accumulation's);
+//   2. dhidden += (-w_t 2^-15) (G W16_c)  A = G (K-major), B = W16_c read in
 //                                          place (MN-major);
-//   3. dW[c]   += 2^-15 (G^T h')          A = G read in place (MN-major),
+//   3. dW[c]   += -2^-15 (G^T h')         A = G read in place (MN-major),
 //                                          B = h' (MN-major).
 // Why the scale: at V = 151,936 nearly every softmax probability is below
 // 2^-14, where fp16 numbers are subnormal and lose relative precision; 2^15 q
@@ -82,10 +82,11 @@ constexpr int STATS_TILES = LM_CHUNK / BN;
 // A/B, three pairs).  The width is a constant: it fixes the order in which a
 // dhidden element accumulates the chunks.
 constexpr int VC = 32768;
-// G holds 2^15 q, q = onehot(y) - p in [-1, 1]: no |q| >= 2^-29 is subnormal
-// in fp16 and |2^15 q| <= 32768 < 65504.
+// G holds -2^15 q, q = onehot(y) - p in [-1, 1]: no |q| >= 2^-29 is subnormal
+// in fp16 and |2^15 q| <= 32768 < 65504.  The accumulation GEMMs multiply by
+// GRAD_UNSCALE = -2^-15 (exact), which restores q and its sign.
 constexpr float GRAD_SCALE = 32768.f;
-constexpr float GRAD_UNSCALE = 1.f / 32768.f;
+constexpr float GRAD_UNSCALE = -1.f / 32768.f;
 constexpr int M_GROUP = 32;        // M tiles sharing the L2-resident slice of A
 // The accumulation GEMMs run with 256-row tiles (TileCfg<true>): measured on
 // their shapes (8192 x 4096 x 16384 and 16384 x 4096 x 8192), 3% and 11%
@@ -196,9 +197,20 @@ __device__ __forceinline__ int unit_tiles(const GemmGeo& g, int un) {
 // so a CTA that finishes early takes more; without one, unit u goes to CTA
 // u mod gridDim.x.  Either way each tile has exactly one CTA computing it over
 // K in a fixed order, so the results do not depend on the schedule.
+// What an epilogue warp hands to its policy besides the accumulator: the
+// problem's output tensor map (for policies that store tiles with TMA), the
+// warp's staging area in shared memory (Epi::kStageBytes) and which half of
+// it is next.
+struct EpiCtx {
+    const CUtensorMap* cmap;
+    uint8_t* stage;
+    uint32_t next;
+};
+
 template <class Epi>
 struct Problem {
     CUtensorMap a, b;
+    CUtensorMap c;  // output map of the epilogue, where it stores tiles by TMA
     GemmGeo g;
     Epi epi;
 };
@@ -273,7 +285,10 @@ struct StatsEpi {
         }
     }
 
-    __device__ void tile(State& st, uint32_t taddr, int /*m*/, int n, int /*row*/) const {
+    static constexpr uint32_t kStageBytes = 0;
+
+    __device__ void tile(State& st, uint32_t taddr, int /*m*/, int n, int /*row*/,
+                         EpiCtx&) const {
         const int64_t col0 = (int64_t)n * BN;
         const int64_t left = V - col0;
         const int ncols = left < BN ? (int)left : BN;
@@ -332,13 +347,18 @@ struct StatsEpi {
     __device__ void unit_end(State& st, int /*m*/, int un, int /*row*/) const {
         if (st.valid) chunk_stats[st.t * n_chunks + un] = make_float4(st.mc, st.sc, st.uc, 0.f);
     }
+
+    __device__ void finish(EpiCtx&, int) const {}
 };
 
 // Backward step 1: the recomputed logits tile becomes the scaled gradient
-// tile 2^15 q = 2^15 (onehot(y) - e^(z - M - ln S)), written as fp16 to
-// G [rows, ldg] (row-major).  Rows past T, columns past V, ignored rows and
-// zero-weight rows are written as +0 (the weight itself is applied by the
-// accumulation GEMMs).
+// tile G = 2^15 (e^(z - M - ln S) - onehot(y)) = -2^15 q, stored as fp16 by
+// TMA through the problem's output map (G [rows, chunk width], row-major).  The scale is folded into the exponent,
+// 2^15 p = 2^((z - M) log2 e + 15 - log2 S): per pair of elements one packed
+// subtract, one packed FMA and two exponentials, and the sign of q is left to
+// the accumulation GEMMs' per-row factor.  Rows past T, columns past V,
+// ignored rows and zero-weight rows are written as +0 (the weight itself is
+// applied by the accumulation GEMMs).
 struct GradEpi {
     int64_t T, V;
     int64_t c0;            // first vocabulary column of this chunk
@@ -346,14 +366,12 @@ struct GradEpi {
     int64_t ignore_index;
     const float* weights;
     const float2* rowstats;
-    __half* G;
-    int64_t ldg;
     int* dev_error;
 
     struct State {
         int64_t t, y;
         bool live;
-        float M, log2S;
+        float M, c15;  // c15 = 15 - log2 S
     };
 
     __device__ void unit_begin(State& st, int m, int /*un*/, int row) const {
@@ -361,14 +379,14 @@ struct GradEpi {
         st.live = false;
         st.y = ignore_index;
         st.M = 0.f;
-        st.log2S = 0.f;
+        st.c15 = 0.f;
         if (st.t < T) {
             st.y = labels ? labels[st.t] : ignore_index;
             const float w = weights ? weights[st.t] : 1.f;
             if (st.y != ignore_index && w != 0.f) {
                 const float2 rs = rowstats[st.t];
                 st.M = rs.x;
-                st.log2S = rs.y * kLog2e;
+                st.c15 = 15.f - rs.y * kLog2e;
                 st.live = true;
                 if (st.y < 0 || st.y >= V || !(rs.x > -INFINITY) || !(rs.y == rs.y)) {
                     st.live = false;  // undefined row: flagged, written as zeros
@@ -380,56 +398,90 @@ struct GradEpi {
         }
     }
 
-    __device__ void tile(State& st, uint32_t taddr, int /*m*/, int n, int /*row*/) const {
+    // Each epilogue warp owns 32 rows of the tile.  Their G values go out 64
+    // columns at a time: written into one half of the warp's staging area
+    // (32 rows x 128 bytes, the 128-byte swizzle: 16-byte chunk c of row r at
+    // chunk c ^ (r & 7)), then stored by one lane with a TMA tensor store that
+    // writes whole 128-byte lines.  A lane writing its own row straight to
+    // global memory would put 32 rows' half sectors in every store.
+    static constexpr uint32_t kHalfBytes = 32 * 128;
+    static constexpr uint32_t kStageBytes = 2 * kHalfBytes;
+
+    __device__ void tile(State& st, uint32_t taddr, int /*m*/, int n, int row,
+                         EpiCtx& ctx) const {
+        const int lane = row & 31;
         const int64_t j0 = (int64_t)n * BN;  // chunk-local column of the tile
+        const int t0 = (int)(st.t - lane);   // first row of this warp
         const uint64_t negM = f2_pack(-st.M, -st.M);
         const uint64_t l2e = f2_pack(kLog2e, kLog2e);
-        const uint64_t nl2s = f2_pack(-st.log2S, -st.log2S);
-        for (int p = 0; p < BN / 32; ++p) {
-            const int64_t jp = j0 + p * 32;
-            float v[32];
-            tmem_ld32(taddr + p * 32, v);
-            tmem_ld_wait();
-            float g[32];
-            if (st.live) {
+        const uint64_t c15 = f2_pack(st.c15, st.c15);
+        for (int pp = 0; pp < BN / 64; ++pp) {
+            uint8_t* half = ctx.stage + (ctx.next & 1u) * kHalfBytes;
+            ++ctx.next;
+            // the store that last read this half (two stores ago) is done reading
+            if (lane == 0) bulk_wait_group_read<1>();
+            __syncwarp();
+            for (int hh = 0; hh < 2; ++hh) {
+                const int p = 2 * pp + hh;
+                const int64_t jp = j0 + p * 32;
+                float v[32];
+                tmem_ld32(taddr + p * 32, v);
+                tmem_ld_wait();
+                float g[32];
+                if (st.live) {
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    const uint64_t d = f2_add(f2_pack(v[i], v[i + 1]), negM);
-                    float a0, a1;
-                    f2_unpack(f2_fma(d, l2e, nl2s), a0, a1);
-                    g[i] = -GRAD_SCALE * ex2_approx(a0);
-                    g[i + 1] = -GRAD_SCALE * ex2_approx(a1);
-                }
-                const int64_t yl = st.y - c0 - jp;
-                if (yl >= 0 && yl < 32) {
+                    for (int i = 0; i < 32; i += 2) {
+                        const uint64_t d = f2_add(f2_pack(v[i], v[i + 1]), negM);
+                        float a0, a1;
+                        f2_unpack(f2_fma(d, l2e, c15), a0, a1);
+                        g[i] = ex2_approx(a0);      // 2^15 p
+                        g[i + 1] = ex2_approx(a1);
+                    }
+                    const int64_t yl = st.y - c0 - jp;
+                    if (yl >= 0 && yl < 32) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (yl == i) g[i] = GRAD_SCALE + g[i];  // 2^15 (1 - p)
-                }
-                const int64_t vcol = c0 + jp;  // vocabulary index of column i is vcol + i
-                if (vcol + 32 > V) {
-                    for (int i = 0; i < 32; ++i)
-                        if (vcol + i >= V) g[i] = 0.f;
-                }
-            } else {
+                        for (int i = 0; i < 32; ++i)
+                            if (yl == i) g[i] = g[i] - GRAD_SCALE;  // 2^15 (p - 1)
+                    }
+                    const int64_t vcol = c0 + jp;  // vocabulary index of column i is vcol + i
+                    if (vcol + 32 > V) {
+                        for (int i = 0; i < 32; ++i)
+                            if (vcol + i >= V) g[i] = 0.f;
+                    }
+                } else {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) g[i] = 0.f;
+                    for (int i = 0; i < 32; ++i) g[i] = 0.f;
+                }
+                uint32_t h2[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const __half2 x = __floats2half2_rn(g[2 * i], g[2 * i + 1]);
+                    h2[i] = *reinterpret_cast<const uint32_t*>(&x);
+                }
+                // 32 fp16 = 4 chunks of this row, chunks 4 hh .. 4 hh + 3
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int c = (4 * hh + i) ^ (lane & 7);
+                    *reinterpret_cast<uint4*>(half + lane * 128 + c * 16) =
+                        make_uint4(h2[4 * i], h2[4 * i + 1], h2[4 * i + 2], h2[4 * i + 3]);
+                }
             }
-            // G row segment: 32 fp16 = 4 x 16 bytes
-            uint32_t h2[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const __half2 x = __floats2half2_rn(g[2 * i], g[2 * i + 1]);
-                h2[i] = *reinterpret_cast<const uint32_t*>(&x);
+            fence_proxy_async_smem();  // the writes above precede the store's reads
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_2d(ctx.cmap, (int)(j0 + pp * 64), t0, half);
+                bulk_commit_group();
             }
-            uint4* gp = reinterpret_cast<uint4*>(G + st.t * ldg + jp);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                gp[i] = make_uint4(h2[4 * i], h2[4 * i + 1], h2[4 * i + 2], h2[4 * i + 3]);
         }
     }
 
     __device__ void unit_end(State&, int, int, int) const {}
+
+    // Every store this warp issued has completed before the CTA ends.
+    __device__ void finish(EpiCtx&, int row) const {
+        if ((row & 31) == 0) bulk_wait_group<0>();
+        __syncwarp();
+    }
 };
 
 // Backward steps 2 and 3: out[row0 + r, c] += f_r acc[r, c] for r < rows,
@@ -449,7 +501,9 @@ struct AccumEpi {
 
     __device__ void unit_begin(State&, int, int, int) const {}
 
-    __device__ void tile(State&, uint32_t taddr, int m, int n, int row) const {
+    static constexpr uint32_t kStageBytes = 0;
+
+    __device__ void tile(State&, uint32_t taddr, int m, int n, int row, EpiCtx&) const {
         const int64_t r = (int64_t)m * BM + row;
         const int64_t c0 = (int64_t)n * BN;
         float f = 0.f;
@@ -469,11 +523,25 @@ struct AccumEpi {
     }
 
     __device__ void unit_end(State&, int, int, int) const {}
+
+    __device__ void finish(EpiCtx&, int) const {}
 };
 
 // ---------------------------------------------------------------------------
 // The GEMM kernel.
 // ---------------------------------------------------------------------------
+// Shared memory of a GEMM kernel instantiation: the tile configuration's
+// layout, then (1 KB aligned) each epilogue warp's staging area.
+template <bool kWide>
+__host__ __device__ constexpr uint32_t stage_offset() {
+    return (TileCfg<kWide>::total + 1023u) & ~1023u;
+}
+template <class Epi, bool kWide>
+__host__ __device__ constexpr size_t gemm_smem_bytes() {
+    return stage_offset<kWide>() + (size_t)TileCfg<kWide>::EPI_WARPS * Epi::kStageBytes +
+           1024;  // + alignment slack
+}
+
 template <class Epi, bool kF16, uint32_t kLayout, bool kWide>
 __global__ void __launch_bounds__(TileCfg<kWide>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ Problems<Epi> P, int* __restrict__ dev_error) {
@@ -678,6 +746,10 @@ __global__ void __launch_bounds__(TileCfg<kWide>::THREADS, 1)
         const int row = q * 32 + lane;
         uint32_t tc = 0;
         typename Epi::State st;
+        EpiCtx ctx;
+        ctx.cmap = nullptr;
+        ctx.stage = smem + stage_offset<kWide>() + (uint32_t)(warp - 2) * Epi::kStageBytes;
+        ctx.next = 0;
         for (int64_t i = 0; !failed; ++i) {
             int64_t u = consume_unit(i, false);
             __syncwarp();
@@ -691,6 +763,7 @@ __global__ void __launch_bounds__(TileCfg<kWide>::THREADS, 1)
             unit_coords(pr.g, u - (w ? P.n0 : 0), m, un);
             const int nt = unit_tiles(pr.g, un);
             const int m128 = m * C::HALVES + h;  // this warp's 128-row tile
+            ctx.cmap = &pr.c;
             pr.epi.unit_begin(st, m128, un, row);
             for (int j = 0; j < nt; ++j, ++tc) {
                 const int n = un * pr.g.tiles_per_unit + j;
@@ -704,7 +777,7 @@ __global__ void __launch_bounds__(TileCfg<kWide>::THREADS, 1)
                 }
                 tc_fence_after_sync();
                 pr.epi.tile(st, tmem_base + ((uint32_t)(q * 32) << 16) + (kWide ? h : b) * BN,
-                            m128, n, row);
+                            m128, n, row, ctx);
                 // the accumulator may be overwritten once every epilogue warp arrived
                 tc_fence_before_sync();
                 __syncwarp();
@@ -713,6 +786,7 @@ __global__ void __launch_bounds__(TileCfg<kWide>::THREADS, 1)
             if (failed) break;
             pr.epi.unit_end(st, m128, un, row);
         }
+        P.p[0].epi.finish(ctx, row);
     }
 
     if (failed && dev_error) atomicOr(dev_error, PSTAT_DEV_TIMEOUT);
@@ -860,26 +934,31 @@ template <class Epi, bool kF16, uint32_t kLayout, bool kWide>
 static cudaError_t launch_problems(const Problems<Epi>& P, int* dev_error, int sm_count,
                                    cudaStream_t st) {
     using C = TileCfg<kWide>;
+    constexpr size_t smem = gemm_smem_bytes<Epi, kWide>();
+    static_assert(smem <= 227 * 1024, "shared memory per CTA");
     static ContextSeen configured;
     const cudaError_t e = ensure_smem_optin(
-        reinterpret_cast<const void*>(tc_gemm_kernel<Epi, kF16, kLayout, kWide>),
-        (int)C::SMEM_BYTES, configured);
+        reinterpret_cast<const void*>(tc_gemm_kernel<Epi, kF16, kLayout, kWide>), (int)smem,
+        configured);
     if (e != cudaSuccess) return e;
     if (P.total == 0) return cudaSuccess;
     const int64_t grid = P.total < sm_count ? P.total : sm_count;
     tc_gemm_kernel<Epi, kF16, kLayout, kWide>
-        <<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, st>>>(P, dev_error);
+        <<<(unsigned)grid, C::THREADS, smem, st>>>(P, dev_error);
     return cudaGetLastError();
 }
 
 // One GEMM, static round-robin schedule, both operands K-major, tile
-// configuration kWide (the geometry's M tiles must be TileCfg<kWide>::TM rows).
+// configuration kWide (the geometry's M tiles must be TileCfg<kWide>::TM rows);
+// mc is the epilogue's output map, for epilogues that store by TMA.
 template <class Epi, bool kF16, bool kWide = false>
 static cudaError_t launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmGeo& g,
-                               const Epi& epi, int* dev_error, int sm_count, cudaStream_t st) {
+                               const Epi& epi, int* dev_error, int sm_count, cudaStream_t st,
+                               const CUtensorMap* mc = nullptr) {
     Problems<Epi> P;
     P.p[0].a = ma;
     P.p[0].b = mb;
+    if (mc) P.p[0].c = *mc;
     P.p[0].g = g;
     P.p[0].epi = epi;
     P.p[1] = P.p[0];
@@ -1063,10 +1142,12 @@ int pstat_lmhead_backward(const void* hidden, const void* W, int64_t T, int64_t 
     // dhidden.  MN-major maps (inner coordinate M or N): G for dW (inner =
     // vocabulary), W16 for dhidden (inner = d) and h' for dW (inner = d).
     constexpr int kAccTM = lm::TileCfg<lm::ACC_WIDE>::TM;  // A rows per accumulation tile
-    CUtensorMap map_h, map_w, map_G, map_Gmn, map_W16, map_h16;
+    CUtensorMap map_h, map_w, map_Gst, map_G, map_Gmn, map_W16, map_h16;
     constexpr int kGradTM = lm::TileCfg<lm::GRAD_WIDE>::TM;
     if (!lm::make_map(&map_h, false, hidden, T, d, d, kGradTM) ||
         !lm::make_map(&map_w, false, W, V, d, d, lm::BN) ||
+        // one epilogue warp's store: 32 rows x 64 columns of G
+        !lm::make_map(&map_Gst, true, G, Tp, lm::VC, lm::VC, 32) ||
         !lm::make_map(&map_G, true, G, Tp, lm::VC, lm::VC, kAccTM) ||
         !lm::make_map_mn4d(&map_Gmn, G, Tp, lm::VC, lm::VC, kAccTM) ||
         !lm::make_map_mn4d(&map_W16, W16, wl.Vp, d, d, lm::BN) ||
@@ -1080,8 +1161,6 @@ int pstat_lmhead_backward(const void* hidden, const void* W, int64_t T, int64_t 
     ge.ignore_index = ignore_index;
     ge.weights = weights;
     ge.rowstats = reinterpret_cast<const float2*>(rowstats);
-    ge.G = G;
-    ge.ldg = lm::VC;
     ge.dev_error = dev_error;
 
     const int64_t n_chunks = wl.n_chunks;
@@ -1096,13 +1175,14 @@ int pstat_lmhead_backward(const void* hidden, const void* W, int64_t T, int64_t 
     for (int64_t c = 0; c < n_chunks; ++c) {
         const int64_t c0 = c * lm::VC;
         const int64_t vc = (V - c0) < lm::VC ? (V - c0) : lm::VC;
-        // 1. recompute the chunk's logits -> G = fp16(2^15 q)
+        // 1. recompute the chunk's logits -> G = fp16(-2^15 q)
         ge.c0 = c0;
         const lm::GemmGeo g1 = lm::geo(Tp, vc, d, 1, c0, lm::M_GROUP, 0, kGradTM);
         if (lm::launch_gemm<lm::GradEpi, false, lm::GRAD_WIDE>(map_h, map_w, g1, ge, dev_error,
-                                                               dev.sm_count, st) != cudaSuccess)
+                                                               dev.sm_count, st,
+                                                               &map_Gst) != cudaSuccess)
             return PSTAT_ERR_CUDA;
-        // 2. dhidden += (w 2^-15) G W16_c  and  3. dW[c0 : c0 + vc] += 2^-15 G^T h',
+        // 2. dhidden += (-w 2^-15) G W16_c  and  3. dW[c0 : c0 + vc] += -2^-15 G^T h',
         // in one launch: CTAs claim units of both GEMMs (the longer-K one
         // first) from this chunk's counter, so neither leaves a partial last
         // wave.
