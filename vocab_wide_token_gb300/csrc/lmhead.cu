@@ -286,6 +286,7 @@ struct StatsEpi {
     }
 
     static constexpr uint32_t kStageBytes = 0;
+    static constexpr bool kBEvictFirst = true;  // each W k-block is read in one wave
 
     __device__ void tile(State& st, uint32_t taddr, int /*m*/, int n, int /*row*/,
                          EpiCtx&) const {
@@ -406,6 +407,7 @@ struct GradEpi {
     // global memory would put 32 rows' half sectors in every store.
     static constexpr uint32_t kHalfBytes = 32 * 128;
     static constexpr uint32_t kStageBytes = 2 * kHalfBytes;
+    static constexpr bool kBEvictFirst = true;  // each W k-block is read in one wave
 
     __device__ void tile(State& st, uint32_t taddr, int /*m*/, int n, int row,
                          EpiCtx& ctx) const {
@@ -502,6 +504,10 @@ struct AccumEpi {
     __device__ void unit_begin(State&, int, int, int) const {}
 
     static constexpr uint32_t kStageBytes = 0;
+    // A B slice (K long, 8-16 MB) serves the 9-10 M tiles of a wave, whose CTAs
+    // reach each k-block at different times: left at normal L2 priority it
+    // stays for the later ones.
+    static constexpr bool kBEvictFirst = false;
 
     __device__ void tile(State&, uint32_t taddr, int m, int n, int row, EpiCtx&) const {
         const int64_t r = (int64_t)m * BM + row;
@@ -615,7 +621,7 @@ __global__ void __launch_bounds__(TileCfg<kWide>::THREADS, 1)
         // ---------------- TMA producer ----------------
         if (lane == 0) {
             const uint64_t pol_a = policy_evict_last();
-            const uint64_t pol_b = policy_evict_first();
+            const uint64_t pol_b = Epi::kBEvictFirst ? policy_evict_first() : policy_evict_normal();
             uint32_t it = 0;
             for (int64_t i = 0; !failed; ++i) {
                 int64_t u;
