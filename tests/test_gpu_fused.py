@@ -209,6 +209,29 @@ def test_fused_rows_beyond_the_label_cache(cuda_lib):
                       torch.bfloat16, "rows past the label cache")
 
 
+@pytest.mark.parametrize("dtype,V", [(torch.bfloat16, 300000), (torch.bfloat16, 700000),
+                                     (torch.float32, 150000), (torch.float32, 350000)])
+def test_fused_long_rows(cuda_lib, dtype, V):
+    # 74 and 171 chunks per row (up to 6 and 14 per warp of a CTA), a masked half row
+    # and an ignored label: bit for bit against the two calls, and the oracle
+    # on sampled rows.
+    g = torch.Generator(device="cuda").manual_seed(V)
+    T = 40
+    z = (2.0 * torch.randn(T, V, generator=g, device="cuda")).to(dtype)
+    z[3, V // 2:] = -math.inf
+    y = torch.randint(0, V, (T,), generator=g, device="cuda")
+    y[1] = IGN
+    w = torch.randn(T, generator=g, device="cuda")
+    lp, ent, rs, gg, err = _same_as_two_calls(cuda_lib, z, y, w)
+    assert err == 0
+    rows = np.array([0, 3, 39])
+    zo, yo = to_oracle(z[rows]), y[rows].cpu().numpy()
+    assert_forward_close(lp[rows], ent[rows], oracle.forward(zo, yo, IGN), dtype,
+                         what=f"long rows V={V}")
+    assert_grad_close(gg[rows], oracle.backward(zo, yo, w[rows].double().cpu().numpy(), IGN),
+                      dtype, f"long rows V={V}")
+
+
 def test_fused_tiny_config_against_oracle(cuda_lib):
     from vocab_wide_token_gb300 import inputs
 
