@@ -196,6 +196,9 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
 
     const int nc = plan.n_chunks;
     const int active = nc < kFbWarps ? nc : kFbWarps;  // warps that own chunks of any one row
+    // Forward only: the warps with the fewest chunks per row, [active - n_fold,
+    // active), take turns folding the rows.
+    const int n_fold = nc >= kFbWarps && nc % kFbWarps != 0 ? kFbWarps - nc % kFbWarps : active;
     if (lane == 0) {
         for (int s = 0; s < kFbStages; ++s) mbar_init(&bars[s], 1);
     }
@@ -393,9 +396,11 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
                 // This warp's last chunk of the row.  With the backward, every
                 // warp waits for the fold anyway, so the last warp to get here
                 // folds.  Forward only, nobody waits for it, and the folding
-                // warp would start its next row late every row: warp active-1,
-                // which has the fewest chunks per row, folds every row once
-                // the others' records are in.
+                // warp starts its next row late: a warp with the fewest chunks
+                // per row folds it once the others' records are in, these
+                // warps taking turns row by row (with 38 chunks that is warp
+                // 12 alone, whose row has one chunk less; with a multiple of
+                // 13 chunks every warp, so that no one warp carries every fold).
                 __syncwarp();
                 bool fold_now;
                 if constexpr (kBwd) {
@@ -406,7 +411,7 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
                     }
                     arrived = __shfl_sync(0xFFFFFFFFu, arrived, 0);
                     fold_now = arrived == active - 1;
-                } else if (warp != active - 1) {
+                } else if (warp != active - 1 - (int)(tk.r % n_fold)) {
                     if (lane == 0) mbar_arrive(&recs[b]);  // release: this warp's records
                     fold_now = false;
                 } else {
