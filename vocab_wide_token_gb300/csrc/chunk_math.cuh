@@ -45,6 +45,7 @@ struct Elem;
 template <>
 struct Elem<uint16_t> {  // bf16 bit patterns
     static constexpr int kVec = 8;  // elements per 16-byte vector
+    static constexpr int kChunk = PSTAT_CHUNK_BF16;
     __device__ static uint16_t neg_inf() { return 0xFF80u; }
     __device__ static float to_float(uint16_t v) { return __uint_as_float((uint32_t)v << 16); }
     __device__ static uint4 neg_inf_vec() {
@@ -54,6 +55,7 @@ struct Elem<uint16_t> {  // bf16 bit patterns
 template <>
 struct Elem<float> {
     static constexpr int kVec = 4;
+    static constexpr int kChunk = PSTAT_CHUNK_F32;
     __device__ static float neg_inf() { return -INFINITY; }
     __device__ static float to_float(float v) { return v; }
     __device__ static uint4 neg_inf_vec() {
@@ -115,8 +117,10 @@ __device__ __forceinline__ float hsum2(uint64_t p) {
 // The exponent pass first runs without any clamp.  Only a -inf logit can make
 // it produce NaN (e = 0 times a = -inf); then, and only then, the chunk is
 // redone with every element raised to clamp_floor(m), below which e^(z - m)
-// is 0 in fp32 anyway.  Which pass a chunk takes depends only on its own
-// values, so the result is still a fixed function of the chunk.
+// is 0 in fp32 anyway.  A chunk shorter than a full one, padded with -inf,
+// takes the clamped pass directly.  Which pass a chunk takes depends only on
+// its own values and length, so the result is still a fixed function of the
+// chunk.
 template <bool kClamp>
 __device__ __forceinline__ void exp_sums_bf16(const uint4 (&q)[kVecPerLane], float m, float m2,
                                               float& s_out, float& u_out) {
@@ -155,7 +159,11 @@ __device__ __forceinline__ void exp_sums_bf16(const uint4 (&q)[kVecPerLane], flo
     u_out = u;
 }
 
-__device__ __forceinline__ float4 reduce_regs(const uint4 (&q)[kVecPerLane], uint16_t*) {
+// `len` is the chunk's length: load_chunk_regs pads a shorter chunk with -inf
+// vectors, which would make the unclamped pass NaN, so such a chunk goes
+// straight to the clamped one (the pass it would have ended in).
+__device__ __forceinline__ float4 reduce_regs(const uint4 (&q)[kVecPerLane], uint16_t*,
+                                              int len = PSTAT_CHUNK_BF16) {
     uint32_t a0 = q[0].x, a1 = q[0].y, a2 = q[0].z, a3 = q[0].w;
 #pragma unroll
     for (int j = 1; j < kVecPerLane; ++j) {
@@ -169,14 +177,14 @@ __device__ __forceinline__ float4 reduce_regs(const uint4 (&q)[kVecPerLane], uin
     if (m == -INFINITY) return make_float4(m, 0.f, 0.f, 0.f);  // fully masked chunk
     const float m2 = m * kLog2e;
     const float delta = fmaf(m, kLog2e, -m2);
-    float s, u;
-    exp_sums_bf16<false>(q, m, m2, s, u);
+    float s = 0.f, u = NAN;
+    if (len == PSTAT_CHUNK_BF16) exp_sums_bf16<false>(q, m, m2, s, u);
     if (u != u) exp_sums_bf16<true>(q, m, m2, s, u);  // warp-uniform: the butterfly agrees
     return make_float4(m, s, u * kLn2, delta * kLn2);
 }
 
 // Same for fp32 chunks: 4-element vectors, two packed accumulators per lane.
-__device__ __forceinline__ float4 reduce_regs(const uint4 (&q)[kVecPerLane], float*) {
+__device__ __forceinline__ float4 reduce_regs(const uint4 (&q)[kVecPerLane], float*, int = 0) {
     float a0 = -INFINITY, a1 = -INFINITY;
 #pragma unroll
     for (int j = 0; j < kVecPerLane; ++j) {

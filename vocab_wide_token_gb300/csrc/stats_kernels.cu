@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
             issue(ahead, slot);
             next_item(ahead);
         }
-        const float4 r = reduce_regs(q, (E*)nullptr);
+        const float4 r = reduce_regs(q, (E*)nullptr, len);
         if (lane == 0) out[i0 + j] = r;
         next_item(cur);
     }
