@@ -166,7 +166,9 @@ __device__ __forceinline__ void unpack_vec<float>(const uint4& v, float (&x)[4])
 
 // kBwd = false: pass 1 only (the forward: logprob, entropy, (M, ln S)).
 // kShard (forward only): the per-shard statistics instead of the row outputs.
-template <typename Ein, typename Eout, bool kBwd, bool kShard = false>
+// kShards (with the backward): a plan of several shards, whose rows hold
+// several chunks shorter than a full one.
+template <typename Ein, typename Eout, bool kBwd, bool kShard = false, bool kShards = false>
 __global__ void __launch_bounds__(kFbWarps * 32, 1)
     fwdbwd_kernel(const Ein* __restrict__ logits, int64_t T, int64_t V, int64_t ld,
                   const __grid_constant__ ShardPlan plan, const int64_t* __restrict__ labels,
@@ -390,10 +392,11 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
         const int nvec = (len + kVec - 1) / kVec;
 
         if (cc.pass == 0) {
-            // (The single pass keeps the full-length form for every chunk: the
-            // shortcut for short chunks, which gives the same bits, measured
-            // 0.6% slower on its full-vocabulary workload.)
-            const float4 rec = reduce_regs(q, (Ein*)nullptr, kBwd ? Elem<Ein>::kChunk : len);
+            // A short chunk goes straight to the clamped pass, except in the
+            // single pass over a one-shard plan (one short chunk per row),
+            // where that form measured 0.6% slower (same bits).
+            const float4 rec = reduce_regs(q, (Ein*)nullptr,
+                                           (kBwd && !kShards) ? Elem<Ein>::kChunk : len);
             if (lane == 0) records[b * kFbMaxChunks + tk.g] = rec;
             if (cc.i == cc.cnt - 1) {
                 // This warp's last chunk of the row.  With the backward, every
@@ -565,8 +568,8 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
     }
 }
 
-template <typename Ein, typename Eout, bool kBwd, bool kShard = false>
-cudaError_t launch_fused_t(const Ein* logits, int64_t T, int64_t V, int64_t ld,
+template <typename Ein, typename Eout, bool kBwd, bool kShard = false, bool kShards = false>
+cudaError_t launch_fused_one(const Ein* logits, int64_t T, int64_t V, int64_t ld,
                            const ShardPlan& plan, const int64_t* labels, int64_t ignore_index,
                            const float* weights, float* logprob, float* entropy, float* rowstats,
                            Eout* out, int64_t ld_out, int* dev_error, const DeviceInfo& dev,
@@ -574,14 +577,34 @@ cudaError_t launch_fused_t(const Ein* logits, int64_t T, int64_t V, int64_t ld,
                            int64_t label_offset = 0) {
     static ContextSeen configured;
     const cudaError_t e = ensure_smem_optin(
-        reinterpret_cast<const void*>(fwdbwd_kernel<Ein, Eout, kBwd, kShard>), (int)kFusedSmem,
+        reinterpret_cast<const void*>(fwdbwd_kernel<Ein, Eout, kBwd, kShard, kShards>),
+        (int)kFusedSmem,
         configured);
     if (e != cudaSuccess) return e;
     const int64_t grid = T < dev.sm_count ? T : dev.sm_count;
-    fwdbwd_kernel<Ein, Eout, kBwd, kShard><<<(unsigned)grid, kFbWarps * 32, kFusedSmem, stream>>>(
+    fwdbwd_kernel<Ein, Eout, kBwd, kShard, kShards>
+        <<<(unsigned)grid, kFbWarps * 32, kFusedSmem, stream>>>(
         logits, T, V, ld, plan, labels, ignore_index, weights, logprob, entropy, rowstats, out,
         ld_out, shard_out, label_offset, dev_error);
     return cudaGetLastError();
+}
+
+template <typename Ein, typename Eout, bool kBwd, bool kShard = false>
+cudaError_t launch_fused_t(const Ein* logits, int64_t T, int64_t V, int64_t ld,
+                           const ShardPlan& plan, const int64_t* labels, int64_t ignore_index,
+                           const float* weights, float* logprob, float* entropy, float* rowstats,
+                           Eout* out, int64_t ld_out, int* dev_error, const DeviceInfo& dev,
+                           cudaStream_t stream, float4* shard_out = nullptr,
+                           int64_t label_offset = 0) {
+    if constexpr (kBwd) {
+        if (plan.n_shards > 1)
+            return launch_fused_one<Ein, Eout, kBwd, kShard, true>(
+                logits, T, V, ld, plan, labels, ignore_index, weights, logprob, entropy, rowstats,
+                out, ld_out, dev_error, dev, stream, shard_out, label_offset);
+    }
+    return launch_fused_one<Ein, Eout, kBwd, kShard, false>(
+        logits, T, V, ld, plan, labels, ignore_index, weights, logprob, entropy, rowstats, out,
+        ld_out, dev_error, dev, stream, shard_out, label_offset);
 }
 
 }  // namespace
