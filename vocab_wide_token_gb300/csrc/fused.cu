@@ -581,7 +581,19 @@ cudaError_t launch_fused_one(const Ein* logits, int64_t T, int64_t V, int64_t ld
         (int)kFusedSmem,
         configured);
     if (e != cudaSuccess) return e;
-    const int64_t grid = T < dev.sm_count ? T : dev.sm_count;
+    int64_t cap = dev.sm_count;
+    if constexpr (kBwd && sizeof(Ein) == 4) {
+        // Every CTA holds its current row in L2 between the two passes.  fp32
+        // rows of 608 KB (V = 151,936) on all 152 SMs, 92 MB of the 135.5 MB
+        // L2, missed it in pass 2 (DRAM reads 1.33x the logits).  A sweep of
+        // the grid at T = 8192 put the best near three quarters of the SMs
+        // (114 CTAs: 1.63 against 1.87 ms).  bf16 rows carry twice the
+        // elements per byte and wanted more SMs (304 KB rows: all 152; 600 KB:
+        // 136, 5% ahead of 152), so they keep every SM.
+        const int64_t row_bytes = V * (int64_t)sizeof(Ein);
+        if (2 * row_bytes * dev.sm_count > (int64_t)dev.l2_bytes) cap = dev.sm_count * 3 / 4;
+    }
+    const int64_t grid = T < cap ? T : cap;
     fwdbwd_kernel<Ein, Eout, kBwd, kShard, kShards>
         <<<(unsigned)grid, kFbWarps * 32, kFusedSmem, stream>>>(
         logits, T, V, ld, plan, labels, ignore_index, weights, logprob, entropy, rowstats, out,

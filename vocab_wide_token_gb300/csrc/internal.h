@@ -41,6 +41,7 @@ struct DeviceInfo {
     int sm_count;
     int cc_major, cc_minor;
     int max_smem_optin;
+    int l2_bytes;
 };
 int device_info(DeviceInfo* info);  // PSTAT_OK / PSTAT_ERR_CUDA / PSTAT_ERR_UNSUPPORTED
 

@@ -110,7 +110,8 @@ int device_info(DeviceInfo* info) {
             cudaDeviceGetAttribute(&di.cc_minor, cudaDevAttrComputeCapabilityMinor, d) !=
                 cudaSuccess ||
             cudaDeviceGetAttribute(&di.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
-                                   d) != cudaSuccess)
+                                   d) != cudaSuccess ||
+            cudaDeviceGetAttribute(&di.l2_bytes, cudaDevAttrL2CacheSize, d) != cudaSuccess)
             return PSTAT_ERR_CUDA;
         if (d < 64) {
             cache[d] = di;
