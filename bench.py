@@ -57,6 +57,8 @@ def parse():
     p.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
     p.add_argument("--no-lmhead", action="store_true", help="skip the fused lm_head variant")
+    p.add_argument("--no-rows", action="store_true",
+                   help="skip the per-row timings of the other configurations")
     p.add_argument("--lmhead-tokens", type=int, default=16384,
                    help="tokens of the lm_head variant (profiling: smaller)")
     return p.parse_args()
@@ -434,6 +436,10 @@ def main():
         line["lmhead"] = bench_lmhead(pstat, dev, tflops, tflops_sus, peak_kind,
                                       T=args.lmhead_tokens)
 
+    # ---- the other rows and configurations, each timed alone ------------------
+    if not args.no_rows:
+        line["rows"] = bench_rows(pstat, dev, hbm, peak_kind, z, y, rs)
+
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N=1 only) ------
     if rank == 0 and world == 1 and not args.no_cpu:
         import oracle
@@ -484,6 +490,92 @@ def sample_parity(pstat, oracle, zs, ys, ws_, dev):
             "max_abs_entropy_err": float(np.max(np.abs(ent.double().cpu().numpy() - ref["entropy"]))),
             "dlogits_max_excess_over_bf16_rule": float(np.max(np.abs(a - br) - allow)),
             "batch_invariant_rows": len(probes), "batch_invariant": bool(invariant)}
+
+
+def bench_rows(pstat, dev, hbm, peak_kind, z8, y8, rs8, steps=50):
+    """The rows and configurations besides the headline step, each timed alone
+    with CUDA events on the launching stream (device-resident inputs larger
+    than L2, mean over `steps` launches after 3 warm-up launches).  Bytes are
+    algorithmic; fractions are against the measured HBM copy bandwidth.
+      forward_T4096   pstat_forward (one kernel) on the forward-only
+                      configuration: T=4096, 10% of rows with one logit +15;
+      uneven_{bf16,f32}  pstat_forward and pstat_forward_backward with the
+                      3-shard plan (50000 / 50000 / 51936), 10% of the
+                      vocabulary at -inf on 25% of rows, 5% ignored labels,
+                      unit weights; dlogits in the logits' dtype;
+      log_softmax     pstat_log_softmax on the headline workload from its
+                      (M, ln S), bf16 out;
+      policy          the loss-side epilogue on T=8192 tokens:
+                      pstat_logprob_diff_metrics + pstat_clipped_surrogate."""
+    import torch
+    from vocab_wide_token_gb300 import inputs
+
+    stream = torch.cuda.current_stream(dev)
+    err = pstat.new_error_flag(dev)
+
+    def timed(fn, n=steps):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
+    def hbm_row(workload, T, ms, nbytes, launches):
+        gbs = nbytes / (ms / 1e3) / 1e9
+        return {"workload": workload, "ms": ms, "tokens_per_s": T / (ms / 1e3), "gbs": gbs,
+                "frac": gbs / hbm, "peak_kind": peak_kind, "algorithmic_bytes": nbytes,
+                "gpu_launches_per_call": launches}
+
+    out = {}
+    d = inputs.forward_workload(1, dev)
+    z, y = d["logits"], d["labels"]
+    T = z.shape[0]
+    o = (torch.empty(T, device=dev), torch.empty(T, device=dev), torch.empty(T, 2, device=dev))
+    ms = timed(lambda: pstat.forward(z, y, -100, out=o, dev_error=err))
+    out["forward_T4096"] = hbm_row(f"forward only: T={T} x V={V} bf16, 10% peaked rows", T, ms,
+                                   T * (2 * V + 8 + 16), 1)
+    del d, z, y
+    for dt, tag in ((torch.bfloat16, "bf16"), (torch.float32, "f32")):
+        d = inputs.uneven_workload(3, dev, dtype=dt)
+        z, y, b = d["logits"], d["labels"], d["shard_bounds"]
+        T, es = z.shape[0], z.element_size()
+        o = (torch.empty(T, device=dev), torch.empty(T, device=dev),
+             torch.empty(T, 2, device=dev))
+        g = torch.empty_like(z)
+        ms_f = timed(lambda: pstat.forward(z, y, -100, b, out=o, dev_error=err))
+        ms_fb = timed(lambda: pstat.forward_backward(z, y, None, -100, b, out=o, dlogits=g,
+                                                     dev_error=err))
+        wl = f"uneven shards {b}: T={T} x V={V} {tag}, masked vocabulary, 5% ignored"
+        out[f"uneven_{tag}_forward"] = hbm_row(wl, T, ms_f, T * (es * V + 8 + 16), 1)
+        out[f"uneven_{tag}_forward_backward"] = hbm_row(wl, T, ms_fb,
+                                                        T * (2 * es * V + 8 + 4 + 16), 1)
+        del d, z, y, g
+    T = z8.shape[0]
+    ls = torch.empty_like(z8)
+    ms = timed(lambda: pstat.log_softmax(z8, rs8, out=ls, dev_error=err))
+    out["log_softmax"] = hbm_row(f"T={T} x V={V} bf16 from (M, ln S), bf16 out", T, ms,
+                                 T * (2 * V + 2 * V + 8), 1)
+    del ls
+    lp = torch.randn(T, device=dev)
+    lp_old = lp + 1e-3 * torch.randn(T, device=dev)
+    adv = torch.randn(T, device=dev)
+
+    def policy():
+        pstat.logprob_diff_metrics(lp, lp_old, y8)
+        pstat.clipped_surrogate(lp, lp_old, adv, y8)
+
+    ms = timed(policy)
+    out["policy"] = {"workload": f"T={T} tokens: logprob_diff_metrics + clipped_surrogate",
+                     "us": ms * 1e3, "gpu_launches_per_call": 2}
+    torch.cuda.synchronize()
+    assert err.item() == 0, f"device error bits {err.item()}"
+    return out
 
 
 def bench_lmhead(pstat, dev, tflops, tflops_sus, peak_kind, T=16384, steps=3, warmup=1):
