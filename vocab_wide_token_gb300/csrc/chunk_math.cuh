@@ -161,9 +161,15 @@ __device__ __forceinline__ void exp_sums_bf16(const uint4 (&q)[kVecPerLane], flo
 
 // `len` is the chunk's length: load_chunk_regs pads a shorter chunk with -inf
 // vectors, which would make the unclamped pass NaN, so such a chunk goes
-// straight to the clamped one (the pass it would have ended in).
+// straight to the clamped one (the pass it would have ended in).  So does any
+// chunk with `clamp_first`: without a -inf in the chunk the two passes give
+// the same bits (every element the clamp raises has e = 0 either way), so the
+// caller may choose by any rule.  *had_inf is set when a full chunk's
+// unclamped pass came out NaN.
 __device__ __forceinline__ float4 reduce_regs(const uint4 (&q)[kVecPerLane], uint16_t*,
-                                              int len = PSTAT_CHUNK_BF16) {
+                                              int len = PSTAT_CHUNK_BF16,
+                                              bool clamp_first = false,
+                                              bool* had_inf = nullptr) {
     uint32_t a0 = q[0].x, a1 = q[0].y, a2 = q[0].z, a3 = q[0].w;
 #pragma unroll
     for (int j = 1; j < kVecPerLane; ++j) {
@@ -178,13 +184,18 @@ __device__ __forceinline__ float4 reduce_regs(const uint4 (&q)[kVecPerLane], uin
     const float m2 = m * kLog2e;
     const float delta = fmaf(m, kLog2e, -m2);
     float s = 0.f, u = NAN;
-    if (len == PSTAT_CHUNK_BF16) exp_sums_bf16<false>(q, m, m2, s, u);
-    if (u != u) exp_sums_bf16<true>(q, m, m2, s, u);  // warp-uniform: the butterfly agrees
+    const bool unclamped = len == PSTAT_CHUNK_BF16 && !clamp_first;
+    if (unclamped) exp_sums_bf16<false>(q, m, m2, s, u);
+    if (u != u) {  // warp-uniform: the butterfly agrees
+        if (had_inf && unclamped) *had_inf = true;
+        exp_sums_bf16<true>(q, m, m2, s, u);
+    }
     return make_float4(m, s, u * kLn2, delta * kLn2);
 }
 
 // Same for fp32 chunks: 4-element vectors, two packed accumulators per lane.
-__device__ __forceinline__ float4 reduce_regs(const uint4 (&q)[kVecPerLane], float*, int = 0) {
+__device__ __forceinline__ float4 reduce_regs(const uint4 (&q)[kVecPerLane], float*, int = 0,
+                                              bool = true, bool* = nullptr) {
     float a0 = -INFINITY, a1 = -INFINITY;
 #pragma unroll
     for (int j = 0; j < kVecPerLane; ++j) {

@@ -330,6 +330,7 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
     bool failed = false;
     RowInfo ri = {{0.f, 0.f, 0.f, 0.f}, 0, 0.f, 0};
     uint4 q[kVecPerLane];  // the chunk being processed; kept across positions for pass 2
+    bool row_inf = false;  // this warp's first chunk of the current row held a -inf
     while (!done(cc)) {
         const Task tk = task_of(cc);
         const bool hold = held(cc);     // data already in q
@@ -392,11 +393,17 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
         const int nvec = (len + kVec - 1) / kVec;
 
         if (cc.pass == 0) {
-            // A short chunk goes straight to the clamped pass, except in the
-            // single pass over a one-shard plan (one short chunk per row),
-            // where that form measured 0.6% slower (same bits).
+            // A short chunk goes straight to the clamped pass, and so does a
+            // warp's later chunk of a row whose first chunk held a -inf (masked
+            // rows hold them throughout), except in the single pass over a
+            // one-shard plan, where that form measured 0.6% slower (same bits).
+            constexpr bool kPredict = !kBwd || kShards;
+            bool had_inf = false;
             const float4 rec = reduce_regs(q, (Ein*)nullptr,
-                                           (kBwd && !kShards) ? Elem<Ein>::kChunk : len);
+                                           kPredict ? len : Elem<Ein>::kChunk,
+                                           kPredict && cc.i > 0 && row_inf,
+                                           kPredict ? &had_inf : nullptr);
+            if (kPredict && cc.i == 0) row_inf = had_inf;
             if (lane == 0) records[b * kFbMaxChunks + tk.g] = rec;
             if (cc.i == cc.cnt - 1) {
                 // This warp's last chunk of the row.  With the backward, every
