@@ -33,7 +33,8 @@ def _close(lp, ent, ref, rows=None):
 
 
 @pytest.mark.parametrize("T,V,d", [(200, 5000, 256), (128, 4096, 64), (1, 300, 128),
-                                   (333, 12345, 512), (257, 9000, 192)])
+                                   (333, 12345, 512), (257, 9000, 192), (300, 40000, 128),
+                                   (97, 65600, 64)])
 def test_lmhead_small(cuda_lib, T, V, d):
     """Ragged token and vocabulary tails, several chunks, short and long K."""
     h, W, y = _draw(T, V, d, 0.1, T + V + d)
@@ -93,10 +94,13 @@ def _frob_rel(a, ref):
 
 
 @pytest.mark.parametrize("T,V,d", [(200, 5000, 256), (128, 4096, 64), (1, 300, 128),
-                                   (333, 12345, 512), (257, 9000, 192)])
+                                   (333, 12345, 512), (257, 9000, 192), (300, 40000, 128),
+                                   (97, 65600, 64)])
 def test_lmhead_backward_small(cuda_lib, T, V, d):
     """dhidden += g W and dW += g^T hidden against float64 numpy; Frobenius-
-    relative <= 1e-3 per tensor; a second call accumulates."""
+    relative <= 1e-3 per tensor; a second call accumulates.  V = 40000 and
+    65600 span two and three 32768-column chunks of the backward, the last
+    one ragged (7232 columns) or narrower than a tile (64 columns)."""
     h, W, y = _draw(T, V, d, 0.1, 3 * T + V + d)
     g = torch.Generator(device="cuda").manual_seed(T + d)
     w = torch.randn(T, generator=g, device="cuda")
