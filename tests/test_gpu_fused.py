@@ -38,9 +38,14 @@ def _same_as_two_calls(pstat, z, y, w, bounds=None, out_dtype=None):
                                              (torch.float32, torch.bfloat16)])
 @pytest.mark.parametrize("V,bounds", [(10007, None), (10007, [0, 513, 6000, 10007]),
                                       (1001, None), (8, None), (7, None), (1, None),
-                                      (30000, None), (70000, None),
+                                      (30000, None), (70000, None), (151936, None),
                                       (151936, [0, 50000, 100000, 151936])])
 def test_fused_bitwise_equals_two_calls(cuda_lib, dtype, out_dtype, V, bounds):
+    # With V = 151936 and one shard, each warp holds 2 or 3 chunks of a row.
+    # Row 5's first third is -inf, so a warp whose first chunk of that row is
+    # masked takes the clamped exponent pass first on its later, unmasked
+    # chunks in the forward, and the unclamped one in the single pass.  The
+    # two must agree bit for bit.
     g = torch.Generator(device="cuda").manual_seed(V + 17)
     T = 300
     z = (2.5 * torch.randn(T, V, generator=g, device="cuda")).float()
