@@ -123,6 +123,27 @@ def test_lmhead_backward_small(cuda_lib, T, V, d):
     assert _frob_rel(dW.double().cpu().numpy(), 2 * rdW) <= 1e-3
 
 
+def test_lmhead_autograd(cuda_lib):
+    """lmhead_policy_stats: the logprob of lmhead_forward, and grads of
+    sum(c logprob) equal to lmhead_backward with weights c, cast to the
+    inputs' dtype, bit for bit; entropy carries no gradient."""
+    T, V, d = 200, 5000, 256
+    h, W, y = _draw(T, V, d, 0.1, 11)
+    y[0] = IGN
+    c = torch.randn(T, generator=torch.Generator(device="cuda").manual_seed(3), device="cuda")
+    lp, ent, rs = cuda_lib.lmhead_forward(h, W, y, IGN)
+    dh, dW = cuda_lib.lmhead_backward(h, W, y, c, rs, IGN)
+    hA = h.detach().clone().requires_grad_(True)
+    WA = W.detach().clone().requires_grad_(True)
+    lpA, entA = cuda_lib.lmhead_policy_stats(hA, WA, y, IGN)
+    assert not entA.requires_grad
+    (lpA * c).sum().backward()
+    torch.cuda.synchronize()
+    assert torch.equal(lpA.detach(), lp) and torch.equal(entA, ent)
+    assert hA.grad.dtype == h.dtype and WA.grad.dtype == W.dtype
+    assert torch.equal(hA.grad, dh.to(h.dtype)) and torch.equal(WA.grad, dW.to(W.dtype))
+
+
 def _row_errors(a, ref):
     """Per row: Frobenius-relative error and max-abs error over the row's
     max-abs reference value."""

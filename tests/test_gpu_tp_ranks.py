@@ -66,10 +66,16 @@ def _rank(rank, world, port, T, V, bounds, dtype_name, seed, outdir):
         lp, ent, rs, got_bounds = tp.tp_forward(zl, y, b0, IGN, dev_error=err)
         g = tp.tp_backward(zl, y, w, rs, b0, V, IGN, dev_error=err)
         lpG, entG, rsG, gG, _ = tp.tp_forward_backward_gather(zl, y, w, b0, IGN, dev_error=err)
+        # autograd: d sum(w logprob) / d logits is this rank's columns of the
+        # weighted backward with weights w
+        zA = zl.detach().clone().requires_grad_(True)
+        lpA, _ = tp.tp_policy_stats(zA, y, b0, IGN)
+        (lpA * w).sum().backward()
         torch.cuda.synchronize()
         torch.save({"bounds": got_bounds, "err": int(err.item()), "lp": lp.cpu(),
                     "ent": ent.cpu(), "rs": rs.cpu(), "g": g.cpu(), "lpG": lpG.cpu(),
-                    "entG": entG.cpu(), "rsG": rsG.cpu(), "gG": gG.contiguous().cpu()},
+                    "entG": entG.cpu(), "rsG": rsG.cpu(), "gG": gG.contiguous().cpu(),
+                    "lpA": lpA.detach().cpu(), "gA": zA.grad.cpu()},
                    os.path.join(outdir, f"rank{rank}.pt"))
     finally:
         dist.destroy_process_group()
@@ -107,6 +113,9 @@ def test_two_ranks_real_kernels(cuda_lib, tmp_path, dtype, T, V, bounds):
         for key, want in (("lp", lp), ("ent", ent), ("rs", rs)):
             assert torch.equal(_bits(res[key]), _bits(want.cpu())), (r, key)
         assert torch.equal(_bits(res["g"]), _bits(gfull[:, b0:b1].cpu())), r
+        # the autograd function over the same path
+        assert torch.equal(_bits(res["lpA"]), _bits(lp.cpu())), r
+        assert torch.equal(_bits(res["gA"]), _bits(gfull[:, b0:b1].cpu())), r
         # full-gather path == the single-process full-vocabulary single pass
         for key, want in (("lpG", lpF), ("entG", entF), ("rsG", rsF)):
             assert torch.equal(_bits(res[key]), _bits(want.cpu())), (r, key)

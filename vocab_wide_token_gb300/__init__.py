@@ -3,8 +3,10 @@
 The computation lives in ``libpstat.so`` (hand-written sm_103a CUDA behind the
 C ABI of ``include/pstat.h``).  ``vocab_wide_token_gb300.pstat`` is its ctypes
 binding; importing it raises when the library has not been built (there is no
-CPU fallback).  ``vocab_wide_token_gb300.inputs`` holds the seeded synthetic
-workloads and ``vocab_wide_token_gb300.build`` the nvcc build.
+CPU fallback).  ``vocab_wide_token_gb300.tp`` runs the vocabulary-parallel
+path over a torch.distributed group, ``vocab_wide_token_gb300.inputs`` holds
+the seeded synthetic workloads and ``vocab_wide_token_gb300.build`` the nvcc
+build.
 """
 
-__all__ = ["pstat", "inputs", "build"]
+__all__ = ["pstat", "tp", "inputs", "build"]

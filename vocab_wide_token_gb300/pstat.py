@@ -682,3 +682,38 @@ class PolicyStats(torch.autograd.Function):
 def policy_stats(logits, labels, ignore_index: int = -100, shard_bounds=None):
     """Differentiable (logprob, entropy) through the CUDA kernels."""
     return PolicyStats.apply(logits, labels, ignore_index, shard_bounds)
+
+
+class LmheadPolicyStats(torch.autograd.Function):
+    """logprob (differentiable in hidden and W) and entropy (a no-grad metric)
+    of every token through the fused lm_head; the logits hidden W^T are never
+    materialised.
+
+    Backward: with g = grad_logprob_t (onehot(y_t) - softmax(z_t)), dhidden =
+    g W and dW = g^T hidden, accumulated in fp32 by the lm_head backward and
+    returned in the dtypes of hidden and W.
+    """
+
+    @staticmethod
+    def forward(ctx, hidden, W, labels, ignore_index=-100):
+        lp, ent, rs = lmhead_forward(hidden, W, labels, ignore_index)
+        ctx.save_for_backward(hidden, W, labels, rs)
+        ctx.ignore_index = ignore_index
+        ctx.mark_non_differentiable(ent)
+        return lp, ent
+
+    @staticmethod
+    def backward(ctx, grad_lp, grad_ent):
+        hidden, W, labels, rs = ctx.saved_tensors
+        need_h, need_w = ctx.needs_input_grad[0], ctx.needs_input_grad[1]
+        if not (need_h or need_w):
+            return None, None, None, None
+        dh, dW = lmhead_backward(hidden, W, labels, grad_lp.float().contiguous(), rs,
+                                 ctx.ignore_index)
+        return (dh.to(hidden.dtype) if need_h else None, dW.to(W.dtype) if need_w else None,
+                None, None)
+
+
+def lmhead_policy_stats(hidden, W, labels, ignore_index: int = -100):
+    """Differentiable (logprob, entropy) of hidden W^T through the fused lm_head."""
+    return LmheadPolicyStats.apply(hidden, W, labels, ignore_index)

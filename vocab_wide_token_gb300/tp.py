@@ -125,3 +125,34 @@ def tp_forward_backward_gather(logits_local: torch.Tensor, labels: torch.Tensor 
                                             dev_error=dev_error)
     rank = bounds.index(vocab_start)
     return lp, ent, rs, g[:, bounds[rank]:bounds[rank + 1]], bounds
+
+
+class TPPolicyStats(torch.autograd.Function):
+    """Vocabulary-parallel logprob (differentiable in this rank's logits) and
+    entropy (a no-grad metric): tp_forward, then in the backward this rank's
+    columns of grad_logprob_t (onehot(y_t) - softmax(z_t)) through tp_backward,
+    with no communication."""
+
+    @staticmethod
+    def forward(ctx, logits_local, labels, vocab_start, ignore_index=-100, group=None):
+        lp, ent, rs, bounds = tp_forward(logits_local, labels, vocab_start, ignore_index, group)
+        ctx.save_for_backward(logits_local, labels, rs)
+        ctx.vocab_start = int(vocab_start)
+        ctx.vocab_total = int(bounds[-1])
+        ctx.ignore_index = ignore_index
+        ctx.mark_non_differentiable(ent)
+        return lp, ent
+
+    @staticmethod
+    def backward(ctx, grad_lp, grad_ent):
+        logits_local, labels, rs = ctx.saved_tensors
+        g = tp_backward(logits_local, labels, grad_lp.float().contiguous(), rs, ctx.vocab_start,
+                        ctx.vocab_total, ctx.ignore_index)
+        return g, None, None, None, None
+
+
+def tp_policy_stats(logits_local: torch.Tensor, labels: torch.Tensor | None, vocab_start: int,
+                    ignore_index: int = -100, group=None):
+    """Differentiable (logprob, entropy) of the vocabulary-sharded logits:
+    every rank gets the same bits, and each rank's gradient is its columns."""
+    return TPPolicyStats.apply(logits_local, labels, vocab_start, ignore_index, group)
