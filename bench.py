@@ -425,10 +425,21 @@ def main():
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": outh.numel() * 4,
                        "steps": Ke, "dlogits": "stays in device memory"}
         ms3 = timed_e2e(gh)
+        d2h = outh.numel() * 4 + gh.numel() * 2
         line["e2e_dlogits_to_host"] = {
             "value": whole_job_rate(T, Ke, world, ms3), "unit": "tokens/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": outh.numel() * 4 + gh.numel() * 2,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": Ke, "dlogits": "copied to pinned host memory inside the timed region"}
+        # The host link in this run: pinned copies of the same buffers in, out
+        # and both ways at once; the e2e forms are bounded by the bytes each
+        # step moves over it.
+        link = host_link(zh, gh, z, g, dev)
+        t_in = h2d / (link["h2d_gbs"] * 1e9)
+        t_both = max(t_in, d2h / (link["d2h_gbs"] * 1e9),
+                     (h2d + d2h) / (link["both_gbs"] * 1e9))
+        line["e2e"]["link_bound_frac"] = t_in / (ms2 / Ke / 1e3)
+        line["e2e_dlogits_to_host"]["link_bound_frac"] = t_both / (ms3 / Ke / 1e3)
+        line["e2e"]["link"] = link
         del zh, gh
 
     # ---- fused lm_head variant (rank 0 reports) ------------------------------
@@ -456,6 +467,35 @@ def main():
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def host_link(zh, gh, z, g, dev, reps=3):
+    """GB/s of pinned host <-> device copies of these buffers: host to device,
+    device to host, and both at once on two streams."""
+    import torch
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) / reps
+
+    s1 = torch.cuda.Stream(dev)
+    s2 = torch.cuda.Stream(dev)
+
+    def both():
+        with torch.cuda.stream(s1):
+            z.copy_(zh, non_blocking=True)
+        with torch.cuda.stream(s2):
+            gh.copy_(g, non_blocking=True)
+
+    nz, ng = zh.numel() * zh.element_size(), gh.numel() * gh.element_size()
+    return {"h2d_gbs": nz / timed(lambda: z.copy_(zh, non_blocking=True)) / 1e9,
+            "d2h_gbs": ng / timed(lambda: gh.copy_(g, non_blocking=True)) / 1e9,
+            "both_gbs": (nz + ng) / timed(both) / 1e9}
 
 
 def sample_parity(pstat, oracle, zs, ys, ws_, dev):
