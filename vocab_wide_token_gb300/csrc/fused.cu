@@ -168,8 +168,11 @@ __device__ __forceinline__ void unpack_vec<float>(const uint4& v, float (&x)[4])
 // kShard (forward only): the per-shard statistics instead of the row outputs.
 // kShards (with the backward): a plan of several shards, whose rows hold
 // several chunks shorter than a full one.
-template <typename Ein, typename Eout, bool kBwd, bool kShard = false, bool kShards = false>
-__global__ void __launch_bounds__(kFbWarps * 32, 1)
+// kOwnFolder (forward only): one more warp, which owns no chunk and folds the
+// rows, for plans in which every chunk-owning warp holds as many chunks.
+template <typename Ein, typename Eout, bool kBwd, bool kShard = false, bool kShards = false,
+          bool kOwnFolder = false>
+__global__ void __launch_bounds__((kFbWarps + (kOwnFolder ? 1 : 0)) * 32, 1)
     fwdbwd_kernel(const Ein* __restrict__ logits, int64_t T, int64_t V, int64_t ld,
                   const __grid_constant__ ShardPlan plan, const int64_t* __restrict__ labels,
                   int64_t ignore_index, const float* __restrict__ weights,
@@ -199,15 +202,17 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
     const int nc = plan.n_chunks;
     const int active = nc < kFbWarps ? nc : kFbWarps;  // warps that own chunks of any one row
     // Forward only: the warps with the fewest chunks per row, [active - n_fold,
-    // active), take turns folding the rows.
+    // active), take turns folding the rows (with kOwnFolder, warp 13 does).
     const int n_fold = nc >= kFbWarps && nc % kFbWarps != 0 ? kFbWarps - nc % kFbWarps : active;
-    if (lane == 0) {
+    if (lane == 0 && (!kOwnFolder || warp < kFbWarps)) {
         for (int s = 0; s < kFbStages; ++s) mbar_init(&bars[s], 1);
     }
     if (threadIdx.x == 0) {
         mbar_init(&ready[0], 1);
         mbar_init(&ready[1], 1);
-        const int others = (nc < kFbWarps ? nc : kFbWarps) - 1;
+        // forward only: the records of the row's other chunk-owning warps
+        // (all of them with a folding warp of its own) are in
+        const int others = kOwnFolder ? active : active - 1;
         mbar_init(&recs[0], others > 0 ? others : 1);
         mbar_init(&recs[1], others > 0 ? others : 1);
         counter[0] = 0;
@@ -234,8 +239,9 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
     // With at least 13 chunks every warp owns chunks of every row, so it
     // arrives for every row's fold and reads every row's statistics before the
     // double-buffered records and row data are reused two rows later.  With
-    // fewer chunks warps without a chunk leave.
-    if (nc < kFbWarps && warp >= nc) return;
+    // fewer chunks warps without a chunk leave (warp 13 of kOwnFolder owns
+    // none and stays: it folds every row as soon as its records are in).
+    if (nc < kFbWarps && warp >= nc && (!kOwnFolder || warp < kFbWarps)) return;
 
     const uint64_t pol_keep = policy_evict_last();
     const uint64_t pol_once = policy_evict_first();
@@ -321,6 +327,87 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
                           keep ? pol_keep : pol_once);
         }
     };
+
+    if constexpr (kOwnFolder) {
+        // The fold of the CTA's r-th row, token row t, whose chunk records are
+        // in records[b]: the row's statistics in the combine kernel's order,
+        // then what pass 2 needs, published on ready[b], then the row outputs.
+        // Called by the forward's folding warp; the chunk loop below writes
+        // the same steps out in place.
+        auto fold_row = [&](int64_t r, int64_t t, int b) {
+            __threadfence_block();
+            // Label, weight and z_y first (for rows past the cache
+            // the z_y load then runs under the fold's arithmetic).
+            const bool cached = r < kFbRowCache;
+            const int64_t y = cached ? lab_s[r] : (labels ? labels[t] : ignore_index);
+            const float w = cached ? wt_s[r] : (weights ? weights[t] : 1.f);
+            const int64_t yl = kShard ? y - label_offset : y;  // the label's column here
+            const bool y_in = y != ignore_index && yl >= 0 && yl < V;
+            float zy = 0.f;
+            if (lane == 0 && y_in)
+                zy = cached ? zy_s[r] : Elem<Ein>::to_float(logits[t * ld + yl]);
+            const float3 st = fold_row_warp(records + b * kFbMaxChunks, plan, lane);
+            if (kShard && lane == 0) {
+                shard_out[t] = make_float4(st.x, st.y, st.z, zy);
+                mbar_arrive(&ready[b]);
+            } else if (lane == 0) {
+                counter[b] = 0;
+                const float M = st.x, S = st.y, U = st.z;
+                // First what pass 2 waits for -- ln S, the row's mode and
+                // its gradient constants -- then publish; the entropy
+                // (a division) and the global stores come after.
+                const bool empty = !(M > -INFINITY);
+                const bool bad = !empty && y != ignore_index && (y < 0 || y >= V);
+                const float lnS = empty ? NAN : logf(S);
+                RowInfo nr;
+                nr.mode = (y == ignore_index || w == 0.f) ? 0 : (empty || bad) ? 1 : 2;
+                nr.gr = nr.mode == 2 ? grad_row(M, lnS, w) : GradRow{0.f, 0.f, 0.f, 0.f};
+                nr.y = y;
+                nr.zy = zy;
+                info[b] = nr;
+                mbar_arrive(&ready[b]);  // release: records, info visible to waiters
+                float H, lp;
+                if (empty) {
+                    H = NAN;
+                    lp = NAN;
+                } else {
+                    H = lnS - U / S;
+                    if (y == ignore_index) {
+                        lp = 0.f;
+                    } else if (bad) {
+                        lp = NAN;
+                        H = NAN;
+                    } else {
+                        lp = (zy - M) - lnS;
+                    }
+                }
+                if (logprob) logprob[t] = lp;
+                if (entropy) entropy[t] = H;
+                if (rowstats) reinterpret_cast<float2*>(rowstats)[t] = make_float2(M, lnS);
+                const int err = (empty ? PSTAT_DEV_EMPTY_ROW : 0) | (bad ? PSTAT_DEV_BAD_LABEL : 0);
+                if (err && dev_error) atomicOr(dev_error, err);
+            }
+        };
+
+        if (warp == kFbWarps) {
+            // The folding warp.  With every chunk warp holding as many chunks
+            // of a row, a chunk warp that folded would wait for the others'
+            // records (warps drift up to two rows apart) and start its next
+            // row late: 3-shard forward 0.465 against 0.411 ms.
+            for (int64_t r = 0; r < nrows; ++r) {
+                const int b = (int)(r & 1);
+                bool ok = mbar_wait_bounded(&recs[b], (uint32_t)((r >> 1) & 1), kWaitLimitNs);
+                ok = __all_sync(0xFFFFFFFFu, ok);
+                if (!ok) {
+                    if (lane == 0 && dev_error) atomicOr(dev_error, PSTAT_DEV_TIMEOUT);
+                    return;
+                }
+                fold_row(r, blockIdx.x + r * gridDim.x, b);
+                __syncwarp();
+            }
+            return;
+        }
+    }
 
     Cursor ci = {0, 0, 0, 0, 0};  // next position to issue
     settle(ci);
@@ -416,11 +503,9 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
                 // This warp's last chunk of the row.  With the backward, every
                 // warp waits for the fold anyway, so the last warp to get here
                 // folds.  Forward only, nobody waits for it, and the folding
-                // warp starts its next row late: a warp with the fewest chunks
-                // per row folds it once the others' records are in, these
-                // warps taking turns row by row (with 38 chunks that is warp
-                // 12 alone, whose row has one chunk less; with a multiple of
-                // 13 chunks every warp, so that no one warp carries every fold).
+                // warp starts its next row late: the row's folding warp (see
+                // n_fold) folds it once the others' records are in; with 38
+                // chunks that is warp 12, whose row has one chunk less.
                 __syncwarp();
                 bool fold_now;
                 if constexpr (kBwd) {
@@ -431,7 +516,7 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
                     }
                     arrived = __shfl_sync(0xFFFFFFFFu, arrived, 0);
                     fold_now = arrived == active - 1;
-                } else if (warp != active - 1 - (int)(tk.r % n_fold)) {
+                } else if (kOwnFolder || warp != active - 1 - (int)(tk.r % n_fold)) {
                     if (lane == 0) mbar_arrive(&recs[b]);  // release: this warp's records
                     fold_now = false;
                 } else {
@@ -445,6 +530,9 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
                     fold_now = true;
                 }
                 if (fold_now) {
+                    // fold_row's steps, written out in place: as a call they
+                    // measured 0.24% slower in the single pass and 1.1% in the
+                    // forward.  The tests compare the two paths bit for bit.
                     __threadfence_block();
                     // Label, weight and z_y first (for rows past the cache
                     // the z_y load then runs under the fold's arithmetic).
@@ -582,7 +670,8 @@ __global__ void __launch_bounds__(kFbWarps * 32, 1)
     }
 }
 
-template <typename Ein, typename Eout, bool kBwd, bool kShard = false, bool kShards = false>
+template <typename Ein, typename Eout, bool kBwd, bool kShard = false, bool kShards = false,
+          bool kOwnFolder = false>
 cudaError_t launch_fused_one(const Ein* logits, int64_t T, int64_t V, int64_t ld,
                            const ShardPlan& plan, const int64_t* labels, int64_t ignore_index,
                            const float* weights, float* logprob, float* entropy, float* rowstats,
@@ -591,7 +680,7 @@ cudaError_t launch_fused_one(const Ein* logits, int64_t T, int64_t V, int64_t ld
                            int64_t label_offset = 0) {
     static ContextSeen configured;
     const cudaError_t e = ensure_smem_optin(
-        reinterpret_cast<const void*>(fwdbwd_kernel<Ein, Eout, kBwd, kShard, kShards>),
+        reinterpret_cast<const void*>(fwdbwd_kernel<Ein, Eout, kBwd, kShard, kShards, kOwnFolder>),
         (int)kFusedSmem,
         configured);
     if (e != cudaSuccess) return e;
@@ -608,8 +697,8 @@ cudaError_t launch_fused_one(const Ein* logits, int64_t T, int64_t V, int64_t ld
         if (2 * row_bytes * dev.sm_count > (int64_t)dev.l2_bytes) cap = dev.sm_count * 3 / 4;
     }
     const int64_t grid = T < cap ? T : cap;
-    fwdbwd_kernel<Ein, Eout, kBwd, kShard, kShards>
-        <<<(unsigned)grid, kFbWarps * 32, kFusedSmem, stream>>>(
+    fwdbwd_kernel<Ein, Eout, kBwd, kShard, kShards, kOwnFolder>
+        <<<(unsigned)grid, (kFbWarps + (kOwnFolder ? 1 : 0)) * 32, kFusedSmem, stream>>>(
         logits, T, V, ld, plan, labels, ignore_index, weights, logprob, entropy, rowstats, out,
         ld_out, shard_out, label_offset, dev_error);
     return cudaGetLastError();
@@ -625,6 +714,13 @@ cudaError_t launch_fused_t(const Ein* logits, int64_t T, int64_t V, int64_t ld,
     if constexpr (kBwd) {
         if (plan.n_shards > 1)
             return launch_fused_one<Ein, Eout, kBwd, kShard, true>(
+                logits, T, V, ld, plan, labels, ignore_index, weights, logprob, entropy, rowstats,
+                out, ld_out, dev_error, dev, stream, shard_out, label_offset);
+    } else {
+        // A warp of its own folds the rows when every chunk-owning warp holds
+        // as many chunks of a row; otherwise the warps with one chunk less do.
+        if (plan.n_chunks < kFbWarps || plan.n_chunks % kFbWarps == 0)
+            return launch_fused_one<Ein, Eout, kBwd, kShard, false, true>(
                 logits, T, V, ld, plan, labels, ignore_index, weights, logprob, entropy, rowstats,
                 out, ld_out, dev_error, dev, stream, shard_out, label_offset);
     }
