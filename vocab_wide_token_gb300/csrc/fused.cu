@@ -23,8 +23,10 @@
 //
 // The same kernel without pass 2 is pstat_forward's one-kernel path (for
 // plans of at most 256 chunks per row): pass 1 with an evict-first hint, and
-// one designated warp folding every row, so that no warp's next row waits for
-// a fold.
+// the rows folded by the warps with one chunk less, or, when every warp holds
+// as many chunks, by a fourteenth warp of its own, so that no warp's next row
+// waits for a fold.  fp32 rows too wide for L2 on every SM run the single pass
+// on three quarters of the SMs.
 #include <cuda_runtime.h>
 
 #include <atomic>
