@@ -38,9 +38,12 @@ def _same_as_two_calls(pstat, z, y, w, bounds=None, out_dtype=None):
                                              (torch.float32, torch.bfloat16)])
 @pytest.mark.parametrize("V,bounds", [(10007, None), (10007, [0, 513, 6000, 10007]),
                                       (1001, None), (8, None), (7, None), (1, None),
-                                      (30000, None), (70000, None), (151936, None),
+                                      (30000, None), (70000, None), (106000, None),
+                                      (151936, None),
                                       (151936, [0, 50000, 100000, 151936])])
 def test_fused_bitwise_equals_two_calls(cuda_lib, dtype, out_dtype, V, bounds):
+    # V = 106000 is 26 bf16 (52 fp32) chunks, 2 (4) per warp: the forward
+    # folds with a warp of its own, as for 39 chunks over three shards.
     # With V = 151936 and one shard, each warp holds 2 or 3 chunks of a row.
     # Row 5's first third is -inf, so a warp whose first chunk of that row is
     # masked takes the clamped exponent pass first on its later, unmasked
